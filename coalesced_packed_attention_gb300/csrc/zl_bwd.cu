@@ -1,0 +1,443 @@
+// Backward kernel of the coalesced attention engine (sm_103a).
+//
+// Gradient of exact softmax attention for every work item, with each item's FINAL
+// output O and global LSE (a k-split shard of theta=(q,h,k) uses its merged group's
+// values, so its dQ is that chunk's contribution and its dK/dV are final; "Zellige",
+// pith.science review, "What carries the argument").  With D_i = rowsum(dO_i * O_i):
+//   P_ij = exp(s_ij - LSE_i),  dS_ij = P_ij (dO_i . V_j - D_i),
+//   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij Q_i,  dQ_i = scale sum_j dS_ij K_j.
+//
+// A tile is 128 KV rows of one head of one item; the CTA keeps K_j, V_j in shared
+// memory and dK_j, dV_j in TMEM while it walks the item's query blocks.  Per block:
+//   S^T  = K Q_i^T      (SMEM x SMEM -> TMEM R0)   lanes = KV rows, columns = queries
+//   dP^T = V dO_i^T     (SMEM x SMEM -> TMEM R1)
+//   softmax warpgroup (thread = KV row): P^T and dS^T in registers; bf16 copies go to
+//   TMEM R0 (P^T in columns [0,64), dS^T in [64,128)) and dS^T to shared memory
+//   dV  += P^T dO_i     (TMEM x SMEM, dO read MN-major)
+//   dK  += dS^T Q_i     (TMEM x SMEM, Q read MN-major)
+//   dQ_i = dS K         (SMEM x SMEM -> TMEM R1; both operands MN-major)
+//   the same warpgroup (thread = query row) adds dQ_i to the fp32 accumulator with
+//   16-byte vector atomics; the scale is applied once when dQ is finalised.
+// TMEM (512 columns): R0 [0,128), R1 [128,256), dV [256,256+d), dK [384,384+d).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "zl_internal.h"
+#include "zl_kernels.h"
+#include "zl_ptx.cuh"
+
+namespace zl {
+
+namespace {
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kBox = 128 * 128;
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ = kV + kTile;             // 2 stages
+  static constexpr int kDO = kQ + 2 * kTile;        // 2 stages
+  static constexpr int kDS = kDO + 2 * kTile;       // [128 kv][128 q] bf16, two 128-byte-swizzled boxes
+  static constexpr int kLD = kDS + 2 * kBox;        // LSE*log2(e) and D for the 128 queries of a block
+  static constexpr int kBar = kLD + 2 * 128 * 4;
+  static constexpr int kNumBars = 2 + 6 + 5 + 4 + 1 + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 64;
+};
+
+constexpr float kLog2eB = 1.44269504088896340736f;
+constexpr float kInfB = __builtin_huge_valf();
+
+__device__ __forceinline__ void rec_err(int32_t* status, volatile int* abort_flag, int code) {
+  *abort_flag = 1;
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      rec_err(status, abort_flag, ZL_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// The per-item dO maps are rewritten in global memory by every backward call.
+__device__ __forceinline__ void tensormap_acquire(const void* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                        const __grid_constant__ CUtensorMap tm_k,
+                                                        const __grid_constant__ CUtensorMap tm_v,
+                                                        const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* kv_full = bar + 0;
+  uint64_t* kv_empty = bar + 1;
+  uint64_t* q_full = bar + 2;     // [2]
+  uint64_t* do_full = bar + 4;    // [2]
+  uint64_t* q_empty = bar + 6;    // [2]
+  uint64_t* sp_full = bar + 8;
+  uint64_t* ds_full = bar + 9;
+  uint64_t* dq_full = bar + 10;
+  uint64_t* dq_empty = bar + 11;
+  uint64_t* kv_done = bar + 12;
+  uint64_t* tile_full = bar + 13;   // [2]
+  uint64_t* tile_empty = bar + 15;  // [2]
+  uint64_t* drain = bar + 17;
+  uint64_t* ld_full = bar + 18;   // LSE / D of a query block staged in shared memory
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  uint32_t* tmem_slot = misc;
+  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(misc + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  float* sLSE = reinterpret_cast<float*>(smem + L::kLD);
+  float* sD = sLSE + 128;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, ZL_ERR_UNSUPPORTED);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full + i, 1);
+      mbar_init(do_full + i, 1);
+      mbar_init(q_empty + i, 1);
+      mbar_init(tile_full + i, 1);
+      mbar_init(tile_empty + i, 1 + 4);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(kv_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(ld_full, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  uint8_t* sK = smem + L::kK;
+  uint8_t* sV = smem + L::kV;
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sDO = smem + L::kDO;
+  uint8_t* sDS = smem + L::kDS;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t tile_it = 0, kt = 0, qit = 0;
+      bool ok = true;
+      while (ok) {
+        const int t = atomicAdd(p.counter, 1);
+        const int tid = t < p.n_tiles ? t : -1;
+        const uint32_t slot = tile_it & 1;
+        if (!bwait(tile_empty + slot, ((tile_it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        ring[slot] = tid;
+        mbar_arrive(tile_full + slot);
+        ++tile_it;
+        if (tid < 0) break;
+        const DevTile tl = p.tiles[tid];
+        const DevItem& it = p.items[tl.item];
+        const int nq = it.q_hi - it.q_lo;
+        const int nqb = (nq + kBlockM - 1) / kBlockM;
+        if (nqb == 0) continue;
+        const CUtensorMap* tm_do = p.do_maps + tl.item;
+        tensormap_acquire(tm_do);
+        if (!bwait(kv_empty, (kt & 1) ^ 1, abort_flag, p.status)) break;
+        ++kt;
+        const int kvrow = (int)it.seq_offset + it.kv_lo + tl.block * kBlockN;
+        mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(sK + c * L::kBox, &tm_k, kv_full, 64 * c, tl.head, kvrow);
+          tma_load_3d(sV + c * L::kBox, &tm_v, kv_full, 64 * c, tl.head, kvrow);
+        }
+        const int hl = tl.head - it.h_lo;
+        for (int ib = 0; ib < nqb; ++ib) {
+          const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
+          if (!bwait(q_empty + st, ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(q_full + st, L::kTile);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sQ + st * L::kTile + c * L::kBox, &tm_q, q_full + st, 64 * c, tl.head,
+                        (int)it.seq_offset + it.q_lo + ib * kBlockM);
+          mbar_arrive_expect_tx(do_full + st, L::kTile);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sDO + st * L::kTile + c * L::kBox, tm_do, do_full + st, 64 * c, hl, ib * kBlockM);
+          ++qit;
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdSq = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t kIdDQ = idesc_bf16(128, D, true, true);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
+                     aDS = smem_u32(sDS);
+      const uint32_t tR0 = tmem, tR1 = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      uint32_t tile_it = 0, kt = 0, qit = 0, nblocks = 0;
+      bool ok = true;
+      while (ok) {
+        const uint32_t slot = tile_it & 1;
+        if (!bwait(tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.status)) break;
+        const int tid = ring[slot];
+        mbar_arrive(tile_empty + slot);
+        ++tile_it;
+        if (tid < 0) break;
+        const DevTile tl = p.tiles[tid];
+        const DevItem& it = p.items[tl.item];
+        const int nqb = (it.q_hi - it.q_lo + kBlockM - 1) / kBlockM;
+        if (nqb == 0) continue;
+        if (!bwait(kv_full, kt & 1, abort_flag, p.status)) break;
+        ++kt;
+        tc_fence_after();
+        for (int ib = 0; ib < nqb; ++ib) {
+          const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
+          if (!bwait(q_full + st, ph, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t aQs = aQ + st * L::kTile, aDOs = aDO + st * L::kTile;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
+            const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
+            mma_ss(tR0, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQs + off, 16, 1024), kIdSq, kk > 0);
+          }
+          if (!bwait(do_full + st, ph, abort_flag, p.status)) { ok = false; break; }
+          if (nblocks > 0 && !bwait(dq_empty, (nblocks - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
+            const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
+            mma_ss(tR1, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDOs + off, 16, 1024), kIdSq, kk > 0);
+          }
+          mma_commit(sp_full);
+          if (!bwait(ds_full, nblocks & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO ; dK += dS^T Q   (K = 128 queries)
+            const uint32_t acc = (ib > 0 || kk > 0) ? 1u : 0u;
+            mma_ts(tdV, tR0 + kk * 8, sdesc_sw128(aDOs + kk * 2048, L::kBox, 1024), kIdKV, acc);
+            mma_ts(tdK, tR0 + 64 + kk * 8, sdesc_sw128(aQs + kk * 2048, L::kBox, 1024), kIdKV, acc);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dQ = dS K   (K = 128 KV rows)
+            mma_ss(tR1, sdesc_sw128(aDS + kk * 2048, L::kBox, 1024), sdesc_sw128(aK + kk * 2048, L::kBox, 1024),
+                   kIdDQ, kk > 0);
+          mma_commit(q_empty + st);
+          mma_commit(dq_full);
+          ++qit;
+          ++nblocks;
+        }
+        if (!ok) break;
+        mma_commit(kv_done);
+        mma_commit(kv_empty);
+      }
+      mma_commit(drain);
+      bwait(drain, 0, abort_flag, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / dQ warpgroup
+    const int t = threadIdx.x;  // KV row of the tile for P/dS, query row of the block for dQ
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const uint32_t aDSrow = smem_u32(sDS) + t * 128;
+    uint32_t tile_it = 0, nblocks = 0, ntiles = 0;
+    for (;;) {
+      const uint32_t slot = tile_it & 1;
+      if (!__all_sync(0xffffffffu, bwait(tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.status))) break;
+      const int tid = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tile_empty + slot);
+      ++tile_it;
+      if (tid < 0) break;
+      const DevTile tl = p.tiles[tid];
+      const DevItem it = p.items[tl.item];
+      const int nq = it.q_hi - it.q_lo, nh = it.h_hi - it.h_lo;
+      const int nkv = it.kv_hi - it.kv_lo;
+      const int nqb = (nq + kBlockM - 1) / kBlockM;
+      const int hl = tl.head - it.h_lo;
+      const int kv_local = tl.block * kBlockN + t;
+      const bool kv_ok = kv_local < nkv;
+      const float* lse_row = p.lse + it.fin_lse_offset + (int64_t)hl * nq;
+      const float* d_row = p.ws_d + it.ws_d_offset + (int64_t)hl * nq;
+      float* dq_base = p.ws_dq + it.ws_dq_offset + (int64_t)hl * D;
+      bool ok = true;
+      float lse_n = kInfB, d_n = 0.f;
+      if (nqb > 0 && t < nq) { lse_n = __ldg(lse_row + t) * kLog2eB; d_n = __ldg(d_row + t); }
+      for (int ib = 0; ib < nqb; ++ib) {
+        // publish this block's LSE / D, prefetch the next block's
+        sLSE[t] = lse_n;
+        sD[t] = d_n;
+        mbar_arrive(ld_full);  // bounded stand-in for a warpgroup barrier
+        if (!__all_sync(0xffffffffu, bwait(ld_full, nblocks & 1, abort_flag, p.status))) { ok = false; break; }
+        const int qn = (ib + 1) * kBlockM + t;
+        lse_n = kInfB; d_n = 0.f;
+        if (ib + 1 < nqb && qn < nq) { lse_n = __ldg(lse_row + qn) * kLog2eB; d_n = __ldg(d_row + qn); }
+
+        if (!__all_sync(0xffffffffu, bwait(sp_full, nblocks & 1, abort_flag, p.status))) { ok = false; break; }
+        tc_fence_after();
+        float pr[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + 32 * c, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            pr[32 * c + e] = kv_ok ? ex2(fmaf(__uint_as_float(u[e]), sl2, -sLSE[32 * c + e])) : 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + 128 + 32 * c, u);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = pr[32 * c + 2 * e] * (__uint_as_float(u[2 * e]) - sD[32 * c + 2 * e]);
+            const float b2 = pr[32 * c + 2 * e + 1] * (__uint_as_float(u[2 * e + 1]) - sD[32 * c + 2 * e + 1]);
+            pk[e] = pack_bf16(a, b2);
+          }
+          tmem_st16(tmem + lane_base + 64 + 16 * c, pk);
+          // dS^T row t -> shared memory, 128-byte swizzle: 16-byte chunk g of box (c>>1)
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int chunk = (c & 1) * 4 + g;
+            const uint32_t addr = aDSrow + (c >> 1) * L::kBox + ((chunk ^ (t & 7)) << 4);
+            st_shared_v4(addr, pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(pr[64 * c + 2 * e], pr[64 * c + 2 * e + 1]);
+          tmem_st32(tmem + lane_base + 32 * c, pk);
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+
+        // dQ of this block: TMEM R1, lane = query row
+        if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.status))) { ok = false; break; }
+        tc_fence_after();
+        const int q_local = ib * kBlockM + t;
+        float* dst = dq_base + (int64_t)q_local * nh * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + 128 + 32 * c, u);
+          tmem_ld_wait();
+          if (q_local < nq) {
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * v4),
+                        make_float4(__uint_as_float(u[4 * v4]), __uint_as_float(u[4 * v4 + 1]),
+                                    __uint_as_float(u[4 * v4 + 2]), __uint_as_float(u[4 * v4 + 3])));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        ++nblocks;
+      }
+      if (!ok) break;
+      // ---- dK, dV of this tile's KV rows
+      if (nqb > 0) {
+        if (!__all_sync(0xffffffffu, bwait(kv_done, ntiles & 1, abort_flag, p.status))) break;
+        ++ntiles;
+        tc_fence_after();
+      }
+      const int64_t row_off = it.dkv_offset + (int64_t)kv_local * nh * D + (int64_t)hl * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t uv[32], uk[32];
+        if (nqb > 0) {
+          tmem_ld32(tmem + lane_base + 256 + 32 * c, uv);
+          tmem_ld32(tmem + lane_base + 384 + 32 * c, uk);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) uv[e] = uk[e] = 0u;
+        }
+        if (kv_ok) {
+          float4* dv4 = reinterpret_cast<float4*>(p.dv + row_off + 32 * c);
+          float4* dk4 = reinterpret_cast<float4*>(p.dk + row_off + 32 * c);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4) {
+            dv4[v4] = make_float4(__uint_as_float(uv[4 * v4]), __uint_as_float(uv[4 * v4 + 1]),
+                                  __uint_as_float(uv[4 * v4 + 2]), __uint_as_float(uv[4 * v4 + 3]));
+            dk4[v4] = make_float4(__uint_as_float(uk[4 * v4]) * p.scale, __uint_as_float(uk[4 * v4 + 1]) * p.scale,
+                                  __uint_as_float(uk[4 * v4 + 2]) * p.scale, __uint_as_float(uk[4 * v4 + 3]) * p.scale);
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const BwdParams& p, int num_sms, cudaStream_t stream) {
+  const int smem = head_dim == 128 ? BwdLayout<128>::kBytes : BwdLayout<64>::kBytes;
+  const int smem_launch = smem > 120 * 1024 ? smem : 120 * 1024;
+  static bool configured[2] = {false, false};
+  const int di = head_dim == 128 ? 1 : 0;
+  if (!configured[di]) {
+    cudaError_t e = head_dim == 128
+                        ? cudaFuncSetAttribute(zl_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_launch)
+                        : cudaFuncSetAttribute(zl_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_launch);
+    if (e != cudaSuccess) return e;
+    configured[di] = true;
+  }
+  const int grid = p.n_tiles < num_sms ? p.n_tiles : num_sms;
+  if (grid == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream);
+  if (e != cudaSuccess) return e;
+  if (head_dim == 128)
+    zl_bwd_kernel<128><<<grid, 192, smem_launch, stream>>>(tq, tk, tv, p);
+  else
+    zl_bwd_kernel<64><<<grid, 192, smem_launch, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace zl

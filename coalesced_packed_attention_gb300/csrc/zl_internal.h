@@ -1,0 +1,80 @@
+// Internal tables shared by the host planner and the kernels.
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/zl.h"
+
+namespace zl {
+
+constexpr int kBlockM = 128;   // query rows per forward tile / per backward q-step
+constexpr int kBlockN = 128;   // KV rows per forward step / per backward tile
+
+// Resolved work item as the kernels read it (device copy of the planner's table).
+struct DevItem {
+  int64_t seq_offset;
+  int32_t seq_len, q_lo, q_hi, h_lo, h_hi, kv_lo, kv_hi, emit_lse;
+  int64_t out_offset;      // own O block: `o` (bf16) or `o_partial` (fp32)
+  int64_t lse_offset;      // own LSE block in `lse`
+  int64_t fin_out_offset;  // final O / dO block in `o` (group's block for k-split items)
+  int64_t fin_lse_offset;  // final LSE block in `lse`
+  int64_t dq_offset;       // [|q|,|h|,d] block in dq
+  int64_t dkv_offset;      // [|kv|,|h|,d] block in dk and dv
+  int64_t ws_d_offset;     // row sums D, [|h|,|q|] floats in the workspace
+  int64_t ws_dq_offset;    // fp32 dQ accumulator, [|q|,|h|,d] floats in the workspace
+  int64_t rowhead_begin;   // prefix of |q|*|h| over items (row-parallel kernels)
+};
+
+struct DevTile {           // one scheduler unit
+  int32_t item, head, block, cost;
+};
+
+struct DevGroup {          // one k-split merge group
+  int32_t member_begin, n_members, nq, nh;
+  int64_t out_offset;      // merged O block in `o`
+  int64_t lse_offset;      // merged LSE block in `lse`
+  int64_t rowhead_begin;   // prefix of nq*nh over groups
+};
+
+struct DevMember {         // one partial of a merge group
+  int64_t o_offset;        // [nq, nh, d] block in o_partial
+  int64_t lse_offset;      // [nh, nq] block in lse_partial
+};
+
+// Scheduler counters and the status word live in one small device block.
+enum CounterSlot { kCtrFwd = 0, kCtrBwd = 1, kStatus = 2, kNumCounters = 8 };
+
+}  // namespace zl
+
+struct zl_plan {
+  int32_t n_heads = 0, head_dim = 0;
+  int64_t total_tokens = 0;
+  int device = -1;
+  int num_sms = 0;
+  bool host_only = false;
+
+  std::vector<zl::DevItem> items;
+  std::vector<zl_work_item> resolved;
+  std::vector<int32_t> item_group;
+  std::vector<zl::DevTile> fwd_tiles, bwd_tiles;
+  std::vector<zl::DevGroup> groups;
+  std::vector<zl::DevMember> members;
+  std::vector<int32_t> member_items;
+
+  int64_t o_elems = 0, o_partial_elems = 0, lse_elems = 0, dq_elems = 0, dkv_elems = 0;
+  int64_t ws_d_floats = 0, ws_dq_floats = 0, workspace_bytes = 0;
+  int64_t total_rowheads = 0, group_rowheads = 0;
+
+  // device copies (one allocation, carved)
+  void* dev_blob = nullptr;
+  zl::DevItem* d_items = nullptr;
+  zl::DevTile* d_fwd_tiles = nullptr;
+  zl::DevTile* d_bwd_tiles = nullptr;
+  zl::DevGroup* d_groups = nullptr;
+  zl::DevMember* d_members = nullptr;
+  int32_t* d_counters = nullptr;
+  CUtensorMap* d_do_maps = nullptr;          // per item, rewritten by every backward call
+  std::vector<CUtensorMap> h_do_maps;        // host staging of the same
+};

@@ -1,0 +1,56 @@
+// Launch interfaces of the kernels (host side).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "zl_internal.h"
+
+namespace zl {
+
+struct FwdParams {
+  const DevItem* items;
+  const DevTile* tiles;
+  int32_t n_tiles;
+  int32_t* counter;
+  int32_t* status;
+  __nv_bfloat16* o;
+  float* o_partial;
+  float* lse;
+  float scale_log2;
+};
+
+struct BwdParams {
+  const DevItem* items;
+  const DevTile* tiles;
+  int32_t n_tiles;
+  int32_t* counter;
+  int32_t* status;
+  const float* lse;   // final LSE arena
+  const float* ws_d;  // row sums D (workspace)
+  float* ws_dq;       // fp32 dQ accumulator (workspace)
+  float* dk;
+  float* dv;
+  const CUtensorMap* do_maps;  // per item: its final dO block as [|q|, |h|, d] (device memory)
+  float scale;
+  float scale_log2;
+};
+
+cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdParams& p, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_merge(int head_dim, const DevGroup* groups, int32_t n_groups, const DevMember* members,
+                         int64_t total_rowheads, const float* o_partial, const float* lse_partial,
+                         __nv_bfloat16* o, float* lse_out, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_bwd_pre(int head_dim, const DevItem* items, int32_t n_items, int64_t total_rowheads,
+                           const __nv_bfloat16* o, const __nv_bfloat16* d_o, float* ws_d, float* ws_dq,
+                           int num_sms, cudaStream_t stream);
+
+cudaError_t launch_bwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const BwdParams& p, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_dq_finalize(int head_dim, const DevItem* items, int32_t n_items, int64_t total_rowheads,
+                               const float* ws_dq, float* dq, float scale, int num_sms, cudaStream_t stream);
+
+}  // namespace zl

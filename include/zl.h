@@ -1,0 +1,200 @@
+/*
+ * zl.h — C ABI of the coalesced attention engine (GB300, sm_103a).
+ *
+ * The engine runs, in one fused launch on one GPU, bidirectional (non-causal) DiT
+ * attention over a heterogeneous work list: whole varlen-packed sequences next to
+ * distributed-attention shards, each shard cut by its configuration theta=(q,h,k)
+ * into a query-row range, a head subset and a KV chunk ("Zellige: Moldable Sequence
+ * Placement for Mixed Image-Video DiT Training": newx.sg abstract — the coalesced
+ * attention engine executes whole sequences alongside distributed-attention shards;
+ * pith.science review, "What carries the argument" — theta splits queries, heads and
+ * key/value states, and the engine schedules and fuses whole sequences and shards
+ * on shared ranks).  Attention is exact softmax attention (pith.science review,
+ * "Assumptions": FlashAttention [7]); k-split shards emit a partial O plus its
+ * log-sum-exp, and zl_merge_partials combines them as a ring-attention executor
+ * ([19]) would across ranks.
+ *
+ * Conventions shared by every call
+ *  - Q, K, V, dO are bf16 tensors packed as [T, H, d] (token-major, head, then head
+ *    dim contiguous; row stride H*d elements).  d is 64 or 128.  Every sequence is a
+ *    contiguous run of tokens [seq_offset, seq_offset + seq_len).
+ *  - All ranges are half-open and relative to the item's sequence start.
+ *  - The CALLER owns every device buffer passed in (inputs, outputs, workspace).  The
+ *    library owns a zl_plan: its host copy, its device tile lists, item table and
+ *    status word.  fwd / merge / bwd never allocate.
+ *  - Device pointers must be 16-byte aligned (ZL_ERR_ALIGN otherwise).
+ *  - Every launch is asynchronous on the given stream (a cudaStream_t passed as
+ *    void*; NULL = legacy default stream).  A plan keeps one scheduler counter per
+ *    kernel, so launches that use the same plan must be ordered (one stream, or
+ *    ordered by events).
+ *  - No call throws; every call returns a zl_status.  A launch error is ZL_ERR_CUDA
+ *    and leaves the CUDA error state for the caller to inspect.
+ *  - Plans are bound to the device that was current when zl_plan_worklist ran.
+ *
+ * Output arenas (element offsets; the planner assigns every offset left at -1)
+ *  - o (bf16): one [|q|, |h|, d] block per non-k-split item and per merge group.  An
+ *    item (or group) that covers its whole sequence (all rows, all heads) is placed
+ *    in place, at element seq_offset*H*d, so whole sequences come out packed exactly
+ *    like Q.  Other blocks follow after T*H*d.
+ *  - o_partial (fp32): one [|q|, |h|, d] block per k-split (emit_lse=1) item.
+ *  - lse (fp32, natural log): one [|h|, |q|] block per item and per merge group; a
+ *    whole-sequence block sits at seq_offset*H, other blocks after T*H.
+ *  - dq (fp32): one [|q|, |h|, d] block per item; dk, dv (fp32, same layout as each
+ *    other): one [|kv|, |h|, d] block per item.  Whole items sit in place at
+ *    seq_offset*H*d.  Each item writes only its own blocks, so overlapping shards
+ *    never race; a q-split item's dK/dV and a k-split item's dQ are that shard's
+ *    partial contributions (a distributed run would reduce them across ranks).
+ */
+#ifndef ZL_H
+#define ZL_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ZL_API __attribute__((visibility("default")))
+#else
+#define ZL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ZL_OK = 0,
+  ZL_ERR_INVALID_ARG = 1,  /* bad descriptor, size or null pointer                     */
+  ZL_ERR_ALIGN = 2,        /* pointer or offset breaks the 16-byte rule               */
+  ZL_ERR_CUDA = 3,         /* a CUDA runtime/driver call or kernel launch failed      */
+  ZL_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up (see status word)    */
+  ZL_ERR_UNSUPPORTED = 5,  /* e.g. head_dim not in {64,128}, device is not sm_103     */
+  ZL_ERR_NO_MEMORY = 6     /* plan allocation failed                                  */
+} zl_status;
+
+/* One work-list entry: a whole sequence or a theta=(q,h,k) shard of one sequence.
+ * emit_lse = 1 marks a k-split shard: it writes an fp32 partial O (normalised by its
+ * own chunk's softmax sum) plus its LSE, to be merged.  emit_lse items with the same
+ * (seq_offset, seq_len, q range, h range) form one merge group, in list order.
+ * out_offset: element offset of the item's O block in `o` (emit_lse = 0) or in
+ * `o_partial` (emit_lse = 1); -1 = planner assigns.  Must be a multiple of 8.
+ * lse_offset: element offset of the item's LSE block in `lse`; -1 = planner assigns. */
+typedef struct {
+  int64_t seq_offset;
+  int32_t seq_len;
+  int32_t q_lo, q_hi;
+  int32_t h_lo, h_hi;
+  int32_t kv_lo, kv_hi;
+  int32_t emit_lse;
+  int64_t out_offset;
+  int64_t lse_offset;
+} zl_work_item;
+
+typedef struct zl_plan zl_plan;
+
+/* Flag for zl_plan_worklist: build the host tables only (no device upload).  Such a
+ * plan answers the zl_plan_* queries but cannot be launched. */
+#define ZL_PLAN_HOST_ONLY 1u
+
+/* Validate a work list and build its tile lists (host C++), then upload them to the
+ * current device.
+ *   items[n_items]: descriptors (host memory, read only; not retained).
+ *   n_heads H >= 1, head_dim d in {64, 128}, total_tokens T >= 1 (Q/K/V have T rows).
+ * Tiles: forward = (item, head, 128 query rows); backward = (item, head, 128 KV rows).
+ * Each list is sorted longest-first (cost = KV blocks for forward, query blocks for
+ * backward), ties in work-list order, and a persistent grid of one CTA per SM claims
+ * tiles in that order from an atomic counter.
+ * Errors: ZL_ERR_INVALID_ARG for a range outside its sequence, lo > hi, a head range
+ * outside [0,H), a sequence outside [0,T), a negative offset other than -1, or a merge
+ * group whose KV chunks overlap; ZL_ERR_ALIGN for out_offset not a multiple of 8;
+ * ZL_ERR_UNSUPPORTED for d not in {64,128}; ZL_ERR_NO_MEMORY / ZL_ERR_CUDA on
+ * allocation or copy failure.  On error *out is set to NULL. */
+ZL_API zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items, int32_t n_heads,
+                           int32_t head_dim, int64_t total_tokens, uint32_t flags,
+                           zl_plan** out);
+
+/* Free a plan (host and device parts).  NULL is ignored.  Must not be called while a
+ * launch that uses the plan is still running. */
+ZL_API void zl_plan_destroy(zl_plan* plan);
+
+/* Element counts of every arena the caller must allocate for this plan (any pointer
+ * may be NULL).  workspace_bytes: scratch for zl_coalesced_attn_bwd (row sums D and
+ * the fp32 dQ accumulator). */
+ZL_API zl_status zl_plan_arena_sizes(const zl_plan* plan, int64_t* o_elems, int64_t* o_partial_elems,
+                              int64_t* lse_elems, int64_t* dq_elems, int64_t* dkv_elems,
+                              int64_t* workspace_bytes);
+
+/* Resolved placement of item i: its descriptor with offsets filled in, plus
+ * fin_out_offset / fin_lse_offset (where its FINAL O, dO and LSE live in `o` / `lse`:
+ * its own block, or its merge group's block for an emit_lse item), dq_offset and
+ * dkv_offset (its gradient blocks), and group (merge group index or -1). */
+ZL_API zl_status zl_plan_item(const zl_plan* plan, int32_t i, zl_work_item* resolved,
+                       int64_t* fin_out_offset, int64_t* fin_lse_offset, int64_t* dq_offset,
+                       int64_t* dkv_offset, int32_t* group);
+
+/* Counts: which = 0 forward tiles, 1 backward tiles, 2 merge groups, 3 items. */
+ZL_API zl_status zl_plan_count(const zl_plan* plan, int32_t which, int64_t* count);
+
+/* Copy a tile list to host memory as n x 4 int32 {item, head, block, cost}, in the
+ * order the scheduler hands tiles out.  which = 0 forward, 1 backward. */
+ZL_API zl_status zl_plan_tiles(const zl_plan* plan, int32_t which, int32_t* out, int64_t n);
+
+/* Merge group g: member item ids (up to cap written), member count, and the group's
+ * final O / LSE offsets in `o` / `lse`. */
+ZL_API zl_status zl_plan_group(const zl_plan* plan, int32_t g, int32_t* members, int32_t cap,
+                        int32_t* n_members, int64_t* out_offset, int64_t* lse_offset);
+
+/* Forward: one persistent launch over every forward tile of the plan (sm_103a:
+ * TMA-staged Q/K/V tiles, tcgen05 MMA with TMEM accumulators for S = Q K^T and
+ * O += P V, online softmax with base-2 exponent, LSE epilogue).
+ *   q, k, v: bf16 [T, H, d] device pointers (read only).
+ *   o: bf16 arena (see above) for emit_lse = 0 items; may be NULL if there are none.
+ *   o_partial: fp32 arena for emit_lse = 1 items; may be NULL if there are none.
+ *   lse: fp32 arena; every item writes its LSE block (partial LSE for emit_lse items).
+ *   scale: softmax scale applied to Q K^T (1/sqrt(d) for DiT attention).
+ * Items with an empty KV range write O = 0 and LSE = -inf.  Inputs must be finite.
+ * Tail rows past an item's q_hi are computed from neighbouring tokens but never
+ * stored. */
+ZL_API zl_status zl_coalesced_attn_fwd(const zl_plan* plan, const void* q, const void* k,
+                                const void* v, void* o, float* o_partial, float* lse,
+                                float scale, void* stream);
+
+/* Merge every k-split group of the plan: with M = max_c LSE_c,
+ * LSE = M + ln sum_c exp(LSE_c - M) and O = sum_c exp(LSE_c - LSE) O_c.
+ * Reads o_partial and the members' LSE blocks from lse_partial; writes the group's bf16
+ * O block into o and its LSE block into lse_out (lse_out may equal lse_partial: the
+ * planner keeps member and group blocks disjoint).  A row whose chunks are all empty
+ * gets O = 0, LSE = -inf.  HBM-bound, one warp per (row, head). */
+ZL_API zl_status zl_merge_partials(const zl_plan* plan, const float* o_partial,
+                            const float* lse_partial, void* o, float* lse_out, void* stream);
+
+/* Backward of every item, using each item's FINAL output and LSE (for k-split items,
+ * the merged group's O and global LSE):
+ *   D_i = rowsum(dO_i * O_i);  P_ij = exp(s_ij - LSE_i);  dS_ij = P_ij (dO_i.V_j - D_i);
+ *   dV_j = sum_i P_ij dO_i;  dK_j = scale sum_i dS_ij Q_i;  dQ_i = scale sum_j dS_ij K_j,
+ * every sum over the item's own rows x KV chunk.
+ *   q, k, v: as for the forward.  o, d_o: bf16, `o`-arena layout (final outputs and
+ *   their gradients).  lse: fp32 `lse` arena holding the final LSE blocks.
+ *   dq, dk, dv: fp32 gradient arenas (written, not accumulated).
+ *   workspace: device scratch of zl_plan_arena_sizes' workspace_bytes (16-byte aligned).
+ * Launches: row sums D + zeroing of the dQ accumulator; the persistent tcgen05
+ * backward over (item, head, 128 KV rows) tiles; the dQ finalisation (scale). */
+ZL_API zl_status zl_coalesced_attn_bwd(const zl_plan* plan, const void* q, const void* k,
+                                const void* v, const void* o, const void* d_o,
+                                const float* lse, float* dq, float* dk, float* dv,
+                                void* workspace, float scale, void* stream);
+
+/* Read and clear the plan's device status word (synchronises `stream`).  *device_status
+ * receives ZL_OK or the first error a kernel recorded (ZL_ERR_TIMEOUT when a bounded
+ * wait gave up; the kernel then stopped cleanly instead of hanging). */
+ZL_API zl_status zl_get_device_status(const zl_plan* plan, void* stream, int32_t* device_status);
+
+/* Static text for a status code. */
+ZL_API const char* zl_status_string(zl_status status);
+
+/* Library version, e.g. 100 for 0.1.0. */
+ZL_API int32_t zl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZL_H */

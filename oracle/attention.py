@@ -39,11 +39,16 @@ def _rows(item, rows):
     return np.asarray(rows, dtype=np.int64)
 
 
+def _f64(x):
+    # inputs may be float32 holding the bf16 values (exact); arithmetic is float64
+    return np.asarray(x, dtype=np.float64)
+
+
 def scores(q, k, item, h, rows, scale):
     """s_ij = scale * <Q[s+i, h], K[s+j, h]> for i in rows, j in the item's KV chunk."""
     s0 = item.seq_offset
     cols = np.arange(item.kv_lo, item.kv_hi, dtype=np.int64)
-    return scale * (q[s0 + rows, h, :] @ k[s0 + cols, h, :].T)
+    return scale * (_f64(q[s0 + rows, h, :]) @ _f64(k[s0 + cols, h, :]).T)
 
 
 def forward(q, k, v, item, scale, rows=None):
@@ -65,7 +70,7 @@ def forward(q, k, v, item, scale, rows=None):
     cols = np.arange(item.kv_lo, item.kv_hi, dtype=np.int64)
     blk = max(1, _BLOCK_ELEMS // nkv)
     for hi, h in enumerate(heads):
-        Vh = v[s0 + cols, h, :]
+        Vh = _f64(v[s0 + cols, h, :])
         for r0 in range(0, len(rows), blk):
             rb = rows[r0:r0 + blk]
             S = scores(q, k, item, h, rb, scale)
@@ -123,13 +128,13 @@ def backward_dq(q, k, v, do_rows, o_rows, lse_rows, item, scale, rows):
         return dQ
     blk = max(1, _BLOCK_ELEMS // len(cols))
     for hi, h in enumerate(range(item.h_lo, item.h_hi)):
-        Kh, Vh = k[s0 + cols, h, :], v[s0 + cols, h, :]
+        Kh, Vh = _f64(k[s0 + cols, h, :]), _f64(v[s0 + cols, h, :])
         for r0 in range(0, len(rows), blk):
             sl = slice(r0, r0 + blk)
             S = scores(q, k, item, h, rows[sl], scale)
             P = np.exp(S - lse_rows[hi, sl][:, None])
-            dO = do_rows[sl, hi, :]
-            D = (dO * o_rows[sl, hi, :]).sum(axis=1)
+            dO = _f64(do_rows[sl, hi, :])
+            D = (dO * _f64(o_rows[sl, hi, :])).sum(axis=1)
             dP = dO @ Vh.T
             dS = P * (dP - D[:, None])
             dQ[sl, hi, :] = scale * (dS @ Kh)
@@ -155,15 +160,15 @@ def backward_dkdv(q, k, v, do_all, o_all, lse_all, item, scale, kv_rows=None):
         return dK, dV
     blk = max(1, _BLOCK_ELEMS // len(kv_rows))
     for hi, h in enumerate(range(item.h_lo, item.h_hi)):
-        Kc, Vc = k[s0 + kv_rows, h, :], v[s0 + kv_rows, h, :]
+        Kc, Vc = _f64(k[s0 + kv_rows, h, :]), _f64(v[s0 + kv_rows, h, :])
         for r0 in range(0, len(rows), blk):
             rb = rows[r0:r0 + blk]
             sl = slice(r0, r0 + blk)
-            Qr = q[s0 + rb, h, :]
+            Qr = _f64(q[s0 + rb, h, :])
             S = scale * (Qr @ Kc.T)
             P = np.exp(S - lse_all[hi, sl][:, None])
-            dO = do_all[sl, hi, :]
-            D = (dO * o_all[sl, hi, :]).sum(axis=1)
+            dO = _f64(do_all[sl, hi, :])
+            D = (dO * _f64(o_all[sl, hi, :])).sum(axis=1)
             dP = dO @ Vc.T
             dS = P * (dP - D[:, None])
             dV[:, hi, :] += P.T @ dO

@@ -1,0 +1,158 @@
+"""The C-ABI library loads and exports every entry point include/zl.h declares; the
+host planner's validation, placement and tiling (host-only plans, no GPU)."""
+import os
+import re
+
+import pytest
+
+from coalesced_packed_attention_gb300 import zl
+from coalesced_packed_attention_gb300.workloads import (WorkItem, config_images, config_long_video,
+                                                        config_mixed, config_tiny, merge_groups)
+from tests._lib import ensure_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    return ensure_library()
+
+
+def declared_functions():
+    txt = open(os.path.join(ROOT, "include", "zl.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(zl_[a-z_0-9]+)\s*\(", txt)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "zl_coalesced_attn_fwd" in names and "zl_merge_partials" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(zl.exported_symbols()) == sorted(n for n in names if n in zl.exported_symbols())
+    assert set(names) <= set(zl.exported_symbols()) | set(getattr(zl, "EXTRA_SYMBOLS", []))
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert zl.status_string(s)
+    assert zl.status_string(0) == "ok"
+    assert lib.zl_version() >= 100
+
+
+def host_plan(work):
+    return zl.zl_plan_worklist(work.items, work.n_heads, work.head_dim, work.total_tokens,
+                               flags=zl.ZL_PLAN_HOST_ONLY)
+
+
+@pytest.mark.parametrize("bad", [
+    WorkItem(0, 100, 0, 101, 0, 4, 0, 100),        # q range past the sequence
+    WorkItem(0, 100, 5, 4, 0, 4, 0, 100),          # q_lo > q_hi
+    WorkItem(0, 100, 0, 100, 0, 5, 0, 100),        # head outside [0, H)
+    WorkItem(0, 100, 0, 100, 0, 4, -1, 100),       # negative kv_lo
+    WorkItem(950, 100, 0, 100, 0, 4, 0, 100),      # sequence past T
+    WorkItem(0, 100, 0, 100, 0, 4, 0, 100, 2),     # emit_lse not 0/1
+])
+def test_invalid_items_are_rejected(bad):
+    with pytest.raises(zl.ZlError) as e:
+        zl.zl_plan_worklist([bad], 4, 64, 1000, flags=zl.ZL_PLAN_HOST_ONLY)
+    assert e.value.status == zl.ZL_ERR_INVALID_ARG
+
+
+def test_unsupported_head_dim_and_alignment():
+    with pytest.raises(zl.ZlError) as e:
+        zl.zl_plan_worklist([WorkItem(0, 10, 0, 10, 0, 1, 0, 10)], 1, 96, 10, flags=zl.ZL_PLAN_HOST_ONLY)
+    assert e.value.status == zl.ZL_ERR_UNSUPPORTED
+    with pytest.raises(zl.ZlError) as e:
+        zl.zl_plan_worklist([WorkItem(0, 10, 0, 10, 0, 1, 0, 10, 0, out_offset=4)], 1, 64, 10,
+                            flags=zl.ZL_PLAN_HOST_ONLY)
+    assert e.value.status == zl.ZL_ERR_ALIGN
+
+
+def test_overlapping_k_chunks_are_rejected():
+    items = [WorkItem(0, 100, 0, 100, 0, 2, 0, 60, 1), WorkItem(0, 100, 0, 100, 0, 2, 50, 100, 1)]
+    with pytest.raises(zl.ZlError):
+        zl.zl_plan_worklist(items, 2, 64, 100, flags=zl.ZL_PLAN_HOST_ONLY)
+
+
+@pytest.mark.parametrize("make", [config_tiny, config_images, config_mixed, config_long_video])
+def test_tiles_cover_every_row_head_once_longest_first(make):
+    w = make()
+    p = host_plan(w)
+    tiles = p.tiles(0)
+    seen = {}
+    for (i, h, b, cost) in tiles:
+        it = w.items[i]
+        assert it.h_lo <= h < it.h_hi
+        assert 0 <= b * 128 < max(it.nq, 1)
+        assert cost == -(-it.nkv // 128)
+        key = (i, h, b)
+        assert key not in seen
+        seen[key] = 1
+    expected = sum(it.nh * -(-it.nq // 128) for it in w.items)
+    assert len(tiles) == expected == p.n_fwd_tiles
+    costs = [t[3] for t in tiles]
+    assert costs == sorted(costs, reverse=True)
+    # stable: equal costs keep work-list order
+    for a, b in zip(tiles, tiles[1:]):
+        if a[3] == b[3]:
+            assert (a[0], a[1], a[2]) < (b[0], b[1], b[2])
+    btiles = p.tiles(1)
+    assert len(btiles) == sum(it.nh * -(-it.nkv // 128) for it in w.items) == p.n_bwd_tiles
+
+
+@pytest.mark.parametrize("make", [config_tiny, config_images, config_mixed, config_long_video])
+def test_output_blocks_are_disjoint_and_whole_sequences_packed(make):
+    w = make()
+    p = host_plan(w)
+    H, d, T = w.n_heads, w.head_dim, w.total_tokens
+    o_blocks, op_blocks, l_blocks, dq_blocks, dkv_blocks = [], [], [], [], []
+    for i, it in enumerate(w.items):
+        pl = p.item(i)
+        r = pl.item
+        n = it.nq * it.nh
+        (op_blocks if it.emit_lse else o_blocks).append((r.out_offset, r.out_offset + n * d))
+        l_blocks.append((r.lse_offset, r.lse_offset + n))
+        dq_blocks.append((pl.dq_offset, pl.dq_offset + n * d))
+        dkv_blocks.append((pl.dkv_offset, pl.dkv_offset + it.nkv * it.nh * d))
+        whole = (not it.emit_lse and it.q_lo == 0 and it.q_hi == it.seq_len and it.nh == H
+                 and it.kv_lo == 0 and it.kv_hi == it.seq_len)
+        if whole:
+            assert r.out_offset == it.seq_offset * H * d and r.lse_offset == it.seq_offset * H
+            assert pl.dq_offset == it.seq_offset * H * d == pl.dkv_offset
+    for g in range(p.n_groups):
+        members, oo, lo = p.group(g)
+        it = w.items[members[0]]
+        o_blocks.append((oo, oo + it.nq * it.nh * d))
+        l_blocks.append((lo, lo + it.nq * it.nh))
+        for m in members:
+            assert p.item(m).fin_out_offset == oo and p.item(m).fin_lse_offset == lo
+    assert [p.group(g)[0] for g in range(p.n_groups)] == merge_groups(w.items)
+    for blocks, total in ((o_blocks, p.o_elems), (op_blocks, p.o_partial_elems), (l_blocks, p.lse_elems),
+                          (dq_blocks, p.dq_elems), (dkv_blocks, p.dkv_elems)):
+        blocks = sorted(b for b in blocks if b[1] > b[0])
+        for a, b in zip(blocks, blocks[1:]):
+            assert a[1] <= b[0], (a, b)
+        assert all(b[1] <= total for b in blocks)
+    assert p.workspace_bytes >= 4 * sum(it.nq * it.nh * (d + 1) for it in w.items)
+
+
+def test_whole_sequence_group_lands_packed():
+    w = config_long_video()
+    p = host_plan(w)
+    assert p.n_groups == 1
+    members, oo, lo = p.group(0)
+    assert members == list(range(8))
+    assert oo == 0 and lo == 0   # the video is the first packed sequence
+    assert p.o_elems == w.total_tokens * w.n_heads * w.head_dim
+
+
+def test_flop_counts_of_the_workloads():
+    # 4 |q| |kv| d per head (non-causal forward); backward 2.5x
+    assert config_tiny().fwd_flops() == 4 * 64 * 4 * (64 * 64 + 100 * 100 + 256 * 256 + 512 * 512)
+    assert abs(config_images().fwd_flops() / 1e12 - 1.018) < 1e-3
+    m = config_mixed()
+    assert abs(m.fwd_flops() / 1e12 - 16.69) < 5e-3
+    assert abs(config_mixed(with_complement=False).fwd_flops() / 1e12 - 13.39) < 5e-3
+    assert abs(config_long_video().fwd_flops() / 1e12 - 269.4) < 0.1
+    assert m.bwd_flops() == 5 * m.fwd_flops() // 2

@@ -1,0 +1,62 @@
+"""GPU parity of the forward launch and the merge against the CPU float64 oracle,
+through the C ABI, on work lists the oracle finishes in seconds (several tiles and
+ragged tails), plus degenerate shards."""
+import numpy as np
+import pytest
+
+from coalesced_packed_attention_gb300.workloads import (WorkItem, Workload, config_images, config_long_video,
+                                                        config_mixed, config_tiny, scaled)
+from tests.gpu_util import ATOL_LSE, ATOL_O, Run, check, tiny_edge_items
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_mixed_list_all_rows():
+    r = Run(config_tiny(), seed=0)
+    r.check_forward()
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_tiny_mixed_list_more_seeds(seed):
+    Run(config_tiny(), seed=seed).check_forward()
+
+
+def test_tiny_structured_peaky_softmax():
+    Run(config_tiny(), seed=3, structured=True).check_forward()
+
+
+@pytest.mark.parametrize("factor", [6])
+def test_images_scaled(factor):
+    Run(scaled(config_images(), factor), seed=0).check_forward()
+
+
+@pytest.mark.parametrize("factor", [12])
+def test_mixed_shards_scaled(factor):
+    w = scaled(config_mixed(), factor)
+    Run(w, seed=0).check_forward()
+    Run(w, seed=1, structured=True).check_forward()
+
+
+@pytest.mark.parametrize("factor", [24])
+def test_long_video_k8_scaled(factor):
+    Run(scaled(config_long_video(), factor), seed=0).check_forward()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_degenerate_and_ragged_shards(d):
+    H = 3
+    w = Workload(f"edges_d{d}", H, d, 300, tiny_edge_items(H), d ** -0.5)
+    r = Run(w, seed=4)
+    res = r.check_forward()
+    # the empty-KV item: O = 0 and LSE = -inf exactly
+    assert np.all(r.own_o(3) == 0.0) and np.all(np.isneginf(r.own_lse(3)))
+
+
+def test_whole_sequences_land_packed_like_q():
+    # the packed O of the images list reads as [T, H, d] directly
+    w = scaled(config_images(), 16)
+    r = Run(w, seed=5)
+    r.check_forward()
+    T, H, d = w.total_tokens, w.n_heads, w.head_dim
+    o = r.bufs["o"][: T * H * d].reshape(T, H, d)
+    assert np.isfinite(o).all()
