@@ -1,0 +1,375 @@
+"""Benchmark of the coalesced attention engine: one training step of the mixed image +
+video-shard work list (16 whole 1024-token images plus q-, h- and k-split shards of a
+32760-token video, 24 heads, d=128), through the C ABI.
+
+A step is the whole hot path: forward launch over every tile, LSE merge of the k-split
+group, backward (row sums D, tcgen05 backward, dQ finalisation).  The plan is built once
+outside the timed region.  Metric: algorithmic TFLOP/s of forward + backward
+(4 |q| |kv| d per head forward, 2.5x that backward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the step on its own GPU (the
+path has no exchange step on one GPU); the time is the max over ranks and the value is
+the work of all ranks over that time.  --impl reference times the CPU float64 oracle
+on the host cores instead (bounded row samples of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "coalesced attn TFLOP/s (fwd+bwd training step)"
+UNIT = "TFLOP/s"
+KERNEL_SOURCES = {"zl_bwd_main": "coalesced_packed_attention_gb300/csrc/zl_bwd.cu",
+                  "zl_coalesced_attn_fwd": "coalesced_packed_attention_gb300/csrc/zl_fwd.cu"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(total_ms, ws: int, flops_per_rank: float, steps: int):
+    """Whole-job value over replicas: the slowest rank's time (max over ranks of the
+    timed region) and the work of all ranks.  Returns (TFLOP/s, ms per step)."""
+    import torch
+    t = total_ms.clone() if hasattr(total_ms, "clone") else torch.tensor([float(total_ms)])
+    if ws > 1 and torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_step = float(t.reshape(-1)[0].item()) / steps
+    return ws * flops_per_rank / (ms_step * 1e-3) / 1e12, ms_step
+
+
+def sample_clocks(stop: threading.Event, out: list):
+    q = ("--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    try:
+        p = subprocess.Popen(["nvidia-smi", q, "--format=csv,noheader,nounits", "-lms", "200"],
+                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+    except OSError:
+        return
+    try:
+        while not stop.is_set():
+            line = p.stdout.readline()
+            if not line:
+                break
+            out.append(line.strip())
+    finally:
+        p.terminate()
+
+
+def summarize_clocks(lines, gpu_index):
+    sm, mx, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        f = [x.strip() for x in ln.split(",")]
+        if len(f) < 9 or f[0] != str(gpu_index):
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx = float(f[2])
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+    return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_training_traffic.txt")
+    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    vals = {}
+    for ln in open(path):
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def dO_arena(plan, work, do_tok, device):
+    """dO laid out like the `o` arena: each item's final block gets the matching rows and
+    heads of the [T, H, d] gradient."""
+    import torch
+    d = work.head_dim
+    arena = torch.zeros(max(plan.o_elems, 8), dtype=torch.bfloat16, device=device)
+    for i, it in enumerate(work.items):
+        pl = plan.item(i)
+        n = it.nq * it.nh * d
+        arena[pl.fin_out_offset: pl.fin_out_offset + n] = \
+            do_tok[it.seq_offset + it.q_lo: it.seq_offset + it.q_hi, it.h_lo:it.h_hi].reshape(-1)
+    return arena
+
+
+def cpu_oracle_sample(work, seed=0, rows_per_item=24, heads_per_item=2):
+    """Time the oracle (as it stands) on a bounded sample of the workload: for every item,
+    `rows_per_item` query rows x `heads_per_item` heads, forward + dQ backward.  Returns
+    (TFLOP/s over the sampled algorithmic FLOPs, seconds, description)."""
+    import oracle
+    from coalesced_packed_attention_gb300.workloads import WorkItem, make_inputs
+    q, k, v, do = (x.float().numpy() for x in make_inputs(work.total_tokens, work.n_heads, work.head_dim, seed,
+                                                          with_grad_output=True))
+    rng = np.random.default_rng(seed)
+    flops = 0
+    t0 = time.perf_counter()
+    for it in work.items:
+        if it.nq == 0 or it.nkv == 0:
+            continue
+        sub = WorkItem(it.seq_offset, it.seq_len, it.q_lo, it.q_hi, it.h_lo, min(it.h_hi, it.h_lo + heads_per_item),
+                       it.kv_lo, it.kv_hi, it.emit_lse)
+        rows = it.q_lo + np.sort(rng.choice(it.nq, min(rows_per_item, it.nq), replace=False))
+        O, L = oracle.forward(q, k, v, sub, work.scale, rows=rows)
+        dO = do[it.seq_offset + rows][:, sub.h_lo:sub.h_hi]
+        oracle.backward_dq(q, k, v, dO, O, L, sub, work.scale, rows)
+        flops += int(3.5 * 4 * len(rows) * it.nkv * work.head_dim * sub.nh)
+    dt = time.perf_counter() - t0
+    desc = (f"{rows_per_item} random query rows x {heads_per_item} heads of every item: forward + dQ backward "
+            f"in float64 ({flops / 1e9:.1f} GFLOP algorithmic)")
+    return flops / dt / 1e12, dt, desc
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from coalesced_packed_attention_gb300.workloads import config_training
+    work = config_training()
+    for _ in range(args.warmup):
+        cpu_oracle_sample(work, rows_per_item=4)
+    vals, secs = [], []
+    for s in range(args.steps):
+        v, dt, desc = cpu_oracle_sample(work, seed=s)
+        vals.append(v)
+        secs.append(dt)
+    value = float(np.median(vals))
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * float(np.median(secs)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": work.name, "n_heads": work.n_heads, "head_dim": work.head_dim,
+                   "total_tokens": work.total_tokens, "items": len(work.items)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args):
+    import torch
+    from coalesced_packed_attention_gb300 import zl
+    from coalesced_packed_attention_gb300.workloads import config_training, make_inputs
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    zl.load_library()
+
+    work = config_training()
+    H, d, T, scale = work.n_heads, work.head_dim, work.total_tokens, work.scale
+    F_fwd = work.fwd_flops()
+    F_bwd = work.bwd_flops()
+    F_step = F_fwd + F_bwd
+
+    t_plan = time.perf_counter()
+    plan = zl.zl_plan_worklist(work.items, H, d, T)
+    t_plan = time.perf_counter() - t_plan
+
+    q, k, v, do_tok = make_inputs(T, H, d, seed=rank, with_grad_output=True, device=str(dev))
+    d_o = dO_arena(plan, work, do_tok, dev)
+    bufs = zl.allocate(plan, dev, backward=True)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        zl.zl_coalesced_attn_fwd(plan, q, k, v, bufs["o"], bufs["o_partial"], bufs["lse"], scale, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        zl.zl_merge_partials(plan, bufs["o_partial"], bufs["lse"], bufs["o"], bufs["lse"], stream)
+        if ev is not None:
+            ev[2].record(stream)
+        zl.zl_bwd_preprocess(plan, bufs["o"], d_o, bufs["workspace"], stream)
+        if ev is not None:
+            ev[3].record(stream)
+        zl.zl_bwd_main(plan, q, k, v, d_o, bufs["lse"], bufs["dk"], bufs["dv"], bufs["workspace"], scale, stream)
+        if ev is not None:
+            ev[4].record(stream)
+        zl.zl_bwd_finalize(plan, bufs["dq"], bufs["workspace"], scale, stream)
+        if ev is not None:
+            ev[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    status = zl.zl_get_device_status(plan, stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    clock_lines, stop = [], threading.Event()
+    th = threading.Thread(target=sample_clocks, args=(stop, clock_lines), daemon=True)
+    th.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        torch.distributed.barrier()
+    stop.set()
+    th.join(timeout=2)
+    total_ms = t0.elapsed_time(t1)
+    parts = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in evs])  # ms per stage per step
+    status = zl.zl_get_device_status(plan, stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+    value, ms_step = aggregate(torch.tensor([total_ms], device=dev), ws, F_step, args.steps)
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, d_o))
+        host_out = {n: torch.empty(bufs[n].shape, dtype=bufs[n].dtype, pin_memory=True)
+                    for n in ("o", "lse", "dq", "dk", "dv")}
+        dq_, dk_, dv_, ddo = (torch.empty_like(x) for x in (q, k, v, d_o))
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+        d2h = sum(x.numel() * x.element_size() for x in host_out.values())
+
+        def e2e_step():
+            dq_.copy_(hq, non_blocking=True)
+            dk_.copy_(hk, non_blocking=True)
+            dv_.copy_(hv, non_blocking=True)
+            ddo.copy_(hdo, non_blocking=True)
+            zl.zl_coalesced_attn_fwd(plan, dq_, dk_, dv_, bufs["o"], bufs["o_partial"], bufs["lse"], scale, stream)
+            zl.zl_merge_partials(plan, bufs["o_partial"], bufs["lse"], bufs["o"], bufs["lse"], stream)
+            zl.zl_coalesced_attn_bwd(plan, dq_, dk_, dv_, bufs["o"], ddo, bufs["lse"], bufs["dq"], bufs["dk"],
+                                     bufs["dv"], bufs["workspace"], scale, stream)
+            for n, hb in host_out.items():
+                hb.copy_(bufs[n], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(2, min(args.steps, 5))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_val, e_ms = aggregate(torch.tensor([a.elapsed_time(b)], device=dev), ws, F_step, n_e2e)
+        e2e = {"value": e_val, "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    peaks, peak_kind = measured_peaks()
+    med = np.median(parts, axis=0)
+    fwd_ms, merge_ms, pre_ms, bwd_ms, fin_ms = (float(x) for x in med)
+    # dominant kernel: the tcgen05 backward (largest share of the step)
+    bwd_tf = F_bwd / (bwd_ms * 1e-3) / 1e12
+    fwd_tf = F_fwd / (fwd_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops_sustained"])
+    traffic = recorded_traffic("zl_bwd_main")
+    # algorithmic bytes of the HBM-bound kernels
+    merge_bytes = sum(8 * 0 for _ in [])  # filled below
+    grp_rows = 0
+    for g in range(plan.n_groups):
+        members, _, _ = plan.group(g)
+        it = work.items[members[0]]
+        grp_rows += len(members) * it.nq * it.nh
+        merge_bytes += len(members) * it.nq * it.nh * (4 * d + 4) + it.nq * it.nh * (2 * d + 4)
+    pre_bytes = sum(it.nq * it.nh * (2 * d + 2 * d + 4 + 4 * d) for it in work.items)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": work.name, "n_heads": H, "head_dim": d, "total_tokens": T,
+                       "items": len(work.items), "fwd_tflop": F_fwd / 1e12, "bwd_tflop": F_bwd / 1e12,
+                       "l2": "inputs larger than L2 (Q, K, V, dO 302 MB each)",
+                       "parallelism": f"replicas x{ws}"},
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "stage_ms": {"fwd": fwd_ms, "merge": merge_ms, "bwd_preprocess": pre_ms, "bwd_main": bwd_ms,
+                         "bwd_finalize": fin_ms},
+            "merge_gbs": merge_bytes / (merge_ms * 1e-3) / 1e9 if merge_ms > 0 else None,
+            "bwd_preprocess_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9 if pre_ms > 0 else None,
+            "plan_ms": t_plan * 1e3,
+            "roofline": {"kernel": "zl_bwd_main (tcgen05 backward)", "bound": "tensor", "achieved": bwd_tf,
+                         "peak": peak, "peak_kind": f"{peak_kind} bf16 sustained", "unit": "TFLOP/s",
+                         "frac": bwd_tf / peak, "traffic": traffic,
+                         "fwd": {"achieved": fwd_tf, "frac": fwd_tf / peak}},
+            "gpu_launches": 5 * args.steps,
+            "clocks": summarize_clocks(clock_lines, dev.index or 0),
+        }
+        if e2e is not None:
+            line["e2e"] = e2e
+        if ws == 1 and not args.no_cpu_baseline:
+            v_cpu, dt, desc = cpu_oracle_sample(work)
+            line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                    "sample": desc, "seconds": dt}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -49,6 +49,9 @@ bool make_block_map(CUtensorMap* m, const void* base, int64_t rows, int32_t H, i
 
 bool launchable(const zl_plan* p) { return p && !p->host_only && p->d_items; }
 
+// Spin budget of a bounded device wait: ~0.5 s at 2 GHz; short for the test hook.
+long long wait_limit(const zl_plan* p) { return p->test_withhold ? 20000000LL : 1000000000LL; }
+
 }  // namespace
 
 extern "C" zl_status zl_coalesced_attn_fwd(const zl_plan* p, const void* q, const void* k, const void* v, void* o,
@@ -72,6 +75,8 @@ extern "C" zl_status zl_coalesced_attn_fwd(const zl_plan* p, const void* q, cons
   fp.n_tiles = (int32_t)p->fwd_tiles.size();
   fp.counter = p->d_counters + kCtrFwd;
   fp.status = p->d_counters + kStatus;
+  fp.wait_limit = wait_limit(p);
+  fp.withhold_load = p->test_withhold ? 1 : 0;
   fp.o = static_cast<__nv_bfloat16*>(o);
   fp.o_partial = o_partial;
   fp.lse = lse;
@@ -92,61 +97,84 @@ extern "C" zl_status zl_merge_partials(const zl_plan* p, const float* o_partial,
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
 
+extern "C" zl_status zl_bwd_preprocess(const zl_plan* p, const void* o, const void* d_o, void* workspace,
+                                       void* stream) {
+  if (!launchable(p) || !o || !d_o || (p->workspace_bytes > 0 && !workspace)) return ZL_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(d_o) || !aligned16(workspace)) return ZL_ERR_ALIGN;
+  if (p->items.empty()) return ZL_OK;
+  float* ws_d = static_cast<float*>(workspace);
+  cudaError_t e = launch_bwd_pre(p->head_dim, p->d_items, (int32_t)p->items.size(), p->total_rowheads,
+                                 static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), ws_d,
+                                 ws_d + p->ws_d_floats, p->num_sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
+}
+
+extern "C" zl_status zl_bwd_main(const zl_plan* p, const void* q, const void* k, const void* v, const void* d_o,
+                                 const float* lse, float* dk, float* dv, void* workspace, float scale, void* stream) {
+  if (!launchable(p) || !q || !k || !v || !d_o || !lse || !dk || !dv || (p->workspace_bytes > 0 && !workspace))
+    return ZL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) || !aligned16(lse) || !aligned16(dk) ||
+      !aligned16(dv) || !aligned16(workspace))
+    return ZL_ERR_ALIGN;
+  if (p->bwd_tiles.empty()) return ZL_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUtensorMap tq, tk, tv;
+  if (!make_qkv_map(&tq, q, p->total_tokens, p->n_heads, p->head_dim) ||
+      !make_qkv_map(&tk, k, p->total_tokens, p->n_heads, p->head_dim) ||
+      !make_qkv_map(&tv, v, p->total_tokens, p->n_heads, p->head_dim))
+    return ZL_ERR_CUDA;
+  // dO of item i: its final block in the `o` arena, [|q|, |h|, d] with row stride |h| d
+  zl_plan* mp = const_cast<zl_plan*>(p);
+  for (size_t i = 0; i < p->items.size(); ++i) {
+    const DevItem& it = p->items[i];
+    const int64_t nq = it.q_hi - it.q_lo, nh = it.h_hi - it.h_lo;
+    if (nq == 0 || nh == 0) continue;
+    const void* base = static_cast<const __nv_bfloat16*>(d_o) + it.fin_out_offset;
+    if (!make_block_map(&mp->h_do_maps[i], base, nq, (int32_t)nh, p->head_dim)) return ZL_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(p->d_do_maps, p->h_do_maps.data(), sizeof(CUtensorMap) * p->items.size(),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return ZL_ERR_CUDA;
+  float* ws_d = static_cast<float*>(workspace);
+  BwdParams bp;
+  bp.items = p->d_items;
+  bp.tiles = p->d_bwd_tiles;
+  bp.n_tiles = (int32_t)p->bwd_tiles.size();
+  bp.counter = p->d_counters + kCtrBwd;
+  bp.status = p->d_counters + kStatus;
+  bp.wait_limit = wait_limit(p);
+  bp.lse = lse;
+  bp.ws_d = ws_d;
+  bp.ws_dq = ws_d + p->ws_d_floats;
+  bp.dk = dk;
+  bp.dv = dv;
+  bp.scale = scale;
+  bp.scale_log2 = scale * 1.44269504088896340736f;
+  bp.do_maps = p->d_do_maps;
+  cudaError_t e = launch_bwd(p->head_dim, tq, tk, tv, bp, p->num_sms, st);
+  return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
+}
+
+extern "C" zl_status zl_bwd_finalize(const zl_plan* p, float* dq, void* workspace, float scale, void* stream) {
+  if (!launchable(p) || !dq || (p->workspace_bytes > 0 && !workspace)) return ZL_ERR_INVALID_ARG;
+  if (!aligned16(dq) || !aligned16(workspace)) return ZL_ERR_ALIGN;
+  if (p->items.empty()) return ZL_OK;
+  const float* ws_dq = static_cast<const float*>(workspace) + p->ws_d_floats;
+  cudaError_t e = launch_dq_finalize(p->head_dim, p->d_items, (int32_t)p->items.size(), p->total_rowheads, ws_dq,
+                                     dq, scale, p->num_sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
+}
+
 extern "C" zl_status zl_coalesced_attn_bwd(const zl_plan* p, const void* q, const void* k, const void* v,
                                            const void* o, const void* d_o, const float* lse, float* dq, float* dk,
                                            float* dv, void* workspace, float scale, void* stream) {
   if (!launchable(p) || !q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv ||
       (p->workspace_bytes > 0 && !workspace))
     return ZL_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) || !aligned16(lse) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
-    return ZL_ERR_ALIGN;
-  if (p->items.empty()) return ZL_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* ws_d = static_cast<float*>(workspace);
-  float* ws_dq = ws_d + p->ws_d_floats;
-  const int32_t n_items = (int32_t)p->items.size();
-  cudaError_t e = launch_bwd_pre(p->head_dim, p->d_items, n_items, p->total_rowheads,
-                                 static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), ws_d,
-                                 ws_dq, p->num_sms, st);
-  if (e != cudaSuccess) return ZL_ERR_CUDA;
-  if (!p->bwd_tiles.empty()) {
-    CUtensorMap tq, tk, tv;
-    if (!make_qkv_map(&tq, q, p->total_tokens, p->n_heads, p->head_dim) ||
-        !make_qkv_map(&tk, k, p->total_tokens, p->n_heads, p->head_dim) ||
-        !make_qkv_map(&tv, v, p->total_tokens, p->n_heads, p->head_dim))
-      return ZL_ERR_CUDA;
-    // dO of item i: its final block in the `o` arena, [|q|, |h|, d] with row stride |h| d
-    zl_plan* mp = const_cast<zl_plan*>(p);
-    for (size_t i = 0; i < p->items.size(); ++i) {
-      const DevItem& it = p->items[i];
-      const int64_t nq = it.q_hi - it.q_lo, nh = it.h_hi - it.h_lo;
-      if (nq == 0 || nh == 0) continue;
-      const void* base = static_cast<const __nv_bfloat16*>(d_o) + it.fin_out_offset;
-      if (!make_block_map(&mp->h_do_maps[i], base, nq, (int32_t)nh, p->head_dim)) return ZL_ERR_CUDA;
-    }
-    if (cudaMemcpyAsync(p->d_do_maps, p->h_do_maps.data(), sizeof(CUtensorMap) * p->items.size(),
-                        cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return ZL_ERR_CUDA;
-    BwdParams bp;
-    bp.items = p->d_items;
-    bp.tiles = p->d_bwd_tiles;
-    bp.n_tiles = (int32_t)p->bwd_tiles.size();
-    bp.counter = p->d_counters + kCtrBwd;
-    bp.status = p->d_counters + kStatus;
-    bp.lse = lse;
-    bp.ws_d = ws_d;
-    bp.ws_dq = ws_dq;
-    bp.dk = dk;
-    bp.dv = dv;
-    bp.scale = scale;
-    bp.scale_log2 = scale * 1.44269504088896340736f;
-    bp.do_maps = p->d_do_maps;
-    e = launch_bwd(p->head_dim, tq, tk, tv, bp, p->num_sms, st);
-    if (e != cudaSuccess) return ZL_ERR_CUDA;
-  }
-  e = launch_dq_finalize(p->head_dim, p->d_items, n_items, p->total_rowheads, ws_dq, dq, scale, p->num_sms, st);
-  return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
+  zl_status s = zl_bwd_preprocess(p, o, d_o, workspace, stream);
+  if (s == ZL_OK) s = zl_bwd_main(p, q, k, v, d_o, lse, dk, dv, workspace, scale, stream);
+  if (s == ZL_OK) s = zl_bwd_finalize(p, dq, workspace, scale, stream);
+  return s;
 }
 
 extern "C" zl_status zl_get_device_status(const zl_plan* p, void* stream, int32_t* device_status) {

@@ -54,14 +54,14 @@ __device__ __forceinline__ void rec_err(int32_t* status, volatile int* abort_fla
   atomicCAS(status, 0, code);
 }
 
-__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, long long limit, int32_t* status) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       rec_err(status, abort_flag, ZL_ERR_TIMEOUT);
       return false;
     }
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         const int t = atomicAdd(p.counter, 1);
         const int tid = t < p.n_tiles ? t : -1;
         const uint32_t slot = tile_it & 1;
-        if (!bwait(tile_empty + slot, ((tile_it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        if (!bwait(tile_empty + slot, ((tile_it >> 1) & 1) ^ 1, abort_flag, p.wait_limit, p.status)) break;
         ring[slot] = tid;
         mbar_arrive(tile_full + slot);
         ++tile_it;
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         if (nqb == 0) continue;
         const CUtensorMap* tm_do = p.do_maps + tl.item;
         tensormap_acquire(tm_do);
-        if (!bwait(kv_empty, (kt & 1) ^ 1, abort_flag, p.status)) break;
+        if (!bwait(kv_empty, (kt & 1) ^ 1, abort_flag, p.wait_limit, p.status)) break;
         ++kt;
         const int kvrow = (int)it.seq_offset + it.kv_lo + tl.block * kBlockN;
         mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         const int hl = tl.head - it.h_lo;
         for (int ib = 0; ib < nqb; ++ib) {
           const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
-          if (!bwait(q_empty + st, ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!bwait(q_empty + st, ph ^ 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(q_full + st, L::kTile);
           for (int c = 0; c < D / 64; ++c)
             tma_load_3d(sQ + st * L::kTile + c * L::kBox, &tm_q, q_full + st, 64 * c, tl.head,
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
       bool ok = true;
       while (ok) {
         const uint32_t slot = tile_it & 1;
-        if (!bwait(tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.status)) break;
+        if (!bwait(tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.wait_limit, p.status)) break;
         const int tid = ring[slot];
         mbar_arrive(tile_empty + slot);
         ++tile_it;
@@ -219,12 +219,12 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         const DevItem& it = p.items[tl.item];
         const int nqb = (it.q_hi - it.q_lo + kBlockM - 1) / kBlockM;
         if (nqb == 0) continue;
-        if (!bwait(kv_full, kt & 1, abort_flag, p.status)) break;
+        if (!bwait(kv_full, kt & 1, abort_flag, p.wait_limit, p.status)) break;
         ++kt;
         tc_fence_after();
         for (int ib = 0; ib < nqb; ++ib) {
           const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
-          if (!bwait(q_full + st, ph, abort_flag, p.status)) { ok = false; break; }
+          if (!bwait(q_full + st, ph, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t aQs = aQ + st * L::kTile, aDOs = aDO + st * L::kTile;
 #pragma unroll
@@ -232,8 +232,8 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
             mma_ss(tR0, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQs + off, 16, 1024), kIdSq, kk > 0);
           }
-          if (!bwait(do_full + st, ph, abort_flag, p.status)) { ok = false; break; }
-          if (nblocks > 0 && !bwait(dq_empty, (nblocks - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (!bwait(do_full + st, ph, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+          if (nblocks > 0 && !bwait(dq_empty, (nblocks - 1) & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
             mma_ss(tR1, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDOs + off, 16, 1024), kIdSq, kk > 0);
           }
           mma_commit(sp_full);
-          if (!bwait(ds_full, nblocks & 1, abort_flag, p.status)) { ok = false; break; }
+          if (!bwait(ds_full, nblocks & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO ; dK += dS^T Q   (K = 128 queries)
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         mma_commit(kv_empty);
       }
       mma_commit(drain);
-      bwait(drain, 0, abort_flag, p.status);
+      bwait(drain, 0, abort_flag, p.wait_limit, p.status);
     }
   } else {
     // ------------------------------------------------------------ softmax / dQ warpgroup
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
     uint32_t tile_it = 0, nblocks = 0, ntiles = 0;
     for (;;) {
       const uint32_t slot = tile_it & 1;
-      if (!__all_sync(0xffffffffu, bwait(tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, bwait(tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.wait_limit, p.status))) break;
       const int tid = ring[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(tile_empty + slot);
@@ -299,12 +299,12 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         sLSE[t] = lse_n;
         sD[t] = d_n;
         mbar_arrive(ld_full);  // bounded stand-in for a warpgroup barrier
-        if (!__all_sync(0xffffffffu, bwait(ld_full, nblocks & 1, abort_flag, p.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, bwait(ld_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         const int qn = (ib + 1) * kBlockM + t;
         lse_n = kInfB; d_n = 0.f;
         if (ib + 1 < nqb && qn < nq) { lse_n = __ldg(lse_row + qn) * kLog2eB; d_n = __ldg(d_row + qn); }
 
-        if (!__all_sync(0xffffffffu, bwait(sp_full, nblocks & 1, abort_flag, p.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, bwait(sp_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
         float pr[128];
 #pragma unroll
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         mbar_arrive(ds_full);
 
         // dQ of this block: TMEM R1, lane = query row
-        if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
         const int q_local = ib * kBlockM + t;
         float* dst = dq_base + (int64_t)q_local * nh * D;
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
       if (!ok) break;
       // ---- dK, dV of this tile's KV rows
       if (nqb > 0) {
-        if (!__all_sync(0xffffffffu, bwait(kv_done, ntiles & 1, abort_flag, p.status))) break;
+        if (!__all_sync(0xffffffffu, bwait(kv_done, ntiles & 1, abort_flag, p.wait_limit, p.status))) break;
         ++ntiles;
         tc_fence_after();
       }

@@ -59,7 +59,7 @@ __device__ __forceinline__ void record_error(int32_t* status, volatile int* abor
 }
 
 // Bounded wait that also gives up when another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, long long limit,
                                               int32_t* status) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
@@ -67,7 +67,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   for (;;) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       record_error(status, abort_flag, ZL_ERR_TIMEOUT);
       return false;
     }
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(192, 1)
         const int t = atomicAdd(p.counter, 1);
         const int tid = t < p.n_tiles ? t : -1;
         const uint32_t slot = tile_it & 1;
-        if (!wait_or_abort(b.tile_empty + slot, ((tile_it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        if (!wait_or_abort(b.tile_empty + slot, ((tile_it >> 1) & 1) ^ 1, abort_flag, p.wait_limit, p.status)) break;
         ring[slot] = tid;
         mbar_arrive(b.tile_full + slot);
         ++tile_it;
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(192, 1)
         const int nkv = it.kv_hi - it.kv_lo;
         const int nblk = (nkv + kBlockN - 1) / kBlockN;
         if (nblk == 0) continue;
-        if (!wait_or_abort(b.q_empty, (q_it & 1) ^ 1, abort_flag, p.status)) break;
+        if (!wait_or_abort(b.q_empty, (q_it & 1) ^ 1, abort_flag, p.wait_limit, p.status)) break;
         ++q_it;
         const int row0 = (int)it.seq_offset + it.q_lo + tl.block * kBlockM;
         mbar_arrive_expect_tx(b.q_full, L::kTile);
@@ -166,12 +166,17 @@ __global__ void __launch_bounds__(192, 1)
         bool ok = true;
         for (int j = 0; j < nblk && ok; ++j) {
           const uint32_t s = kv_it % S, ph = (kv_it / S) & 1;
-          ok = wait_or_abort(b.k_empty + s, ph ^ 1, abort_flag, p.status);
+          ok = wait_or_abort(b.k_empty + s, ph ^ 1, abort_flag, p.wait_limit, p.status);
           if (!ok) break;
           mbar_arrive_expect_tx(b.k_full + s, L::kTile);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sK + s * L::kTile + c * L::kBox, &tm_k, b.k_full + s, 64 * c, tl.head, kv0 + j * kBlockN);
-          ok = wait_or_abort(b.v_empty + s, ph ^ 1, abort_flag, p.status);
+          if (p.withhold_load && kv_it == 0) {
+            // test hook: the bytes announced above never arrive, so the MMA warp's
+            // bounded wait runs out and the kernel reports ZL_ERR_TIMEOUT
+          } else {
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(sK + s * L::kTile + c * L::kBox, &tm_k, b.k_full + s, 64 * c, tl.head, kv0 + j * kBlockN);
+          }
+          ok = wait_or_abort(b.v_empty + s, ph ^ 1, abort_flag, p.wait_limit, p.status);
           if (!ok) break;
           mbar_arrive_expect_tx(b.v_full + s, L::kTile);
           for (int c = 0; c < D / 64; ++c)
@@ -192,8 +197,8 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       // O += P_jj V_jj, P read from the S buffer the softmax overwrote with bf16.
       auto issue_pv = [&](uint32_t stage, uint32_t kvph, uint32_t scc, bool first) -> bool {
-        if (!wait_or_abort(b.p_full + (scc & 1), (scc >> 1) & 1, abort_flag, p.status)) return false;
-        if (!wait_or_abort(b.v_full + stage, kvph, abort_flag, p.status)) return false;
+        if (!wait_or_abort(b.p_full + (scc & 1), (scc >> 1) & 1, abort_flag, p.wait_limit, p.status)) return false;
+        if (!wait_or_abort(b.v_full + stage, kvph, abort_flag, p.wait_limit, p.status)) return false;
         tc_fence_after();
         const uint32_t tP = tmem + (scc & 1) * 128;
 #pragma unroll
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(192, 1)
       };
       while (ok) {
         const uint32_t slot = tile_it & 1;
-        if (!wait_or_abort(b.tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.status)) break;
+        if (!wait_or_abort(b.tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.wait_limit, p.status)) break;
         const int tid = ring[slot];
         mbar_arrive(b.tile_empty + slot);
         ++tile_it;
@@ -216,13 +221,13 @@ __global__ void __launch_bounds__(192, 1)
         const DevItem& it = p.items[tl.item];
         const int nblk = (it.kv_hi - it.kv_lo + kBlockN - 1) / kBlockN;
         if (nblk == 0) continue;
-        if (!wait_or_abort(b.q_full, q_it & 1, abort_flag, p.status)) break;
+        if (!wait_or_abort(b.q_full, q_it & 1, abort_flag, p.wait_limit, p.status)) break;
         ++q_it;
         tc_fence_after();
         uint32_t pstage = 0, pph = 0, psc = 0;
         for (int j = 0; j < nblk; ++j) {
           const uint32_t s = kv_it % S, ph = (kv_it / S) & 1;
-          if (!wait_or_abort(b.k_full + s, ph, abort_flag, p.status)) { ok = false; break; }
+          if (!wait_or_abort(b.k_full + s, ph, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tS = tmem + (sc & 1) * 128;
 #pragma unroll
@@ -245,7 +250,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       // make sure no MMA is still writing TMEM before it is released
       mma_commit(b.drain);
-      wait_or_abort(b.drain, 0, abort_flag, p.status);
+      wait_or_abort(b.drain, 0, abort_flag, p.wait_limit, p.status);
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroup
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t tile_it = 0, sc = 0, pv_seen = 0;
     for (;;) {
       const uint32_t slot = tile_it & 1;
-      if (!__all_sync(0xffffffffu, wait_or_abort(b.tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, wait_or_abort(b.tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.wait_limit, p.status))) break;
       const int tid = ring[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(b.tile_empty + slot);
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int j = 0; j < nblk; ++j) {
         const uint32_t buf = sc & 1;
-        if (!__all_sync(0xffffffffu, wait_or_abort(b.s_full + buf, (sc >> 1) & 1, abort_flag, p.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_or_abort(b.s_full + buf, (sc >> 1) & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
         const uint32_t tS = tmem + lane_base + buf * 128;
         float s[128];
@@ -303,7 +308,7 @@ __global__ void __launch_bounds__(192, 1)
         bool waited = false;
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // O holds P_{<j} V; wait for the last PV product before rescaling it
-          if (!__all_sync(0xffffffffu, wait_or_abort(b.o_bar, pv_seen & 1, abort_flag, p.status))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, wait_or_abort(b.o_bar, pv_seen & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
           ++pv_seen;
           waited = true;
           tc_fence_after();
@@ -337,7 +342,7 @@ __global__ void __launch_bounds__(192, 1)
         l += sum;
         tmem_st_wait();
         if (j > 0 && !waited) {
-          if (!__all_sync(0xffffffffu, wait_or_abort(b.o_bar, pv_seen & 1, abort_flag, p.status))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, wait_or_abort(b.o_bar, pv_seen & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
           ++pv_seen;
         }
         tc_fence_before();
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (!ok) break;
       if (nblk > 0) {
-        if (!__all_sync(0xffffffffu, wait_or_abort(b.o_bar, pv_seen & 1, abort_flag, p.status))) break;
+        if (!__all_sync(0xffffffffu, wait_or_abort(b.o_bar, pv_seen & 1, abort_flag, p.wait_limit, p.status))) break;
         ++pv_seen;
         tc_fence_after();
       }

@@ -54,6 +54,7 @@ struct zl_plan {
   int device = -1;
   int num_sms = 0;
   bool host_only = false;
+  bool test_withhold = false;   // ZL_PLAN_TEST_WITHHOLD_LOAD
 
   std::vector<zl::DevItem> items;
   std::vector<zl_work_item> resolved;

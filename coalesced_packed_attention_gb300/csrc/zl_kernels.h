@@ -14,6 +14,8 @@ struct FwdParams {
   int32_t n_tiles;
   int32_t* counter;
   int32_t* status;
+  long long wait_limit;   // cycles a bounded wait may spin
+  int32_t withhold_load;  // test hook: announce but never issue the first K load
   __nv_bfloat16* o;
   float* o_partial;
   float* lse;
@@ -26,6 +28,7 @@ struct BwdParams {
   int32_t n_tiles;
   int32_t* counter;
   int32_t* status;
+  long long wait_limit;
   const float* lse;   // final LSE arena
   const float* ws_d;  // row sums D (workspace)
   float* ws_dq;       // fp32 dQ accumulator (workspace)

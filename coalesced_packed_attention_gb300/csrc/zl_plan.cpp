@@ -253,6 +253,7 @@ extern "C" zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items
   p->head_dim = head_dim;
   p->total_tokens = total_tokens;
   p->host_only = (flags & ZL_PLAN_HOST_ONLY) != 0;
+  p->test_withhold = (flags & ZL_PLAN_TEST_WITHHOLD_LOAD) != 0;
   zl_status s = build(p, items, n_items);
   if (s == ZL_OK && !p->host_only) s = upload(p);
   if (s != ZL_OK) {

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libzl.so")
 
 ZL_OK, ZL_ERR_INVALID_ARG, ZL_ERR_ALIGN, ZL_ERR_CUDA, ZL_ERR_TIMEOUT, ZL_ERR_UNSUPPORTED, ZL_ERR_NO_MEMORY = range(7)
 ZL_PLAN_HOST_ONLY = 1
+ZL_PLAN_TEST_WITHHOLD_LOAD = 2
 
 
 class ZlError(RuntimeError):
@@ -59,6 +60,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "zl_coalesced_attn_fwd": (I32, [P, P, P, P, P, P, P, F, P]),
         "zl_merge_partials": (I32, [P, P, P, P, P, P]),
         "zl_coalesced_attn_bwd": (I32, [P, P, P, P, P, P, P, P, P, P, P, F, P]),
+        "zl_bwd_preprocess": (I32, [P, P, P, P, P]),
+        "zl_bwd_main": (I32, [P, P, P, P, P, P, P, P, P, F, P]),
+        "zl_bwd_finalize": (I32, [P, P, P, F, P]),
         "zl_get_device_status": (I32, [P, P, pI32]),
         "zl_status_string": (ctypes.c_char_p, [I32]),
         "zl_version": (I32, []),
@@ -227,6 +231,31 @@ def zl_coalesced_attn_bwd(plan: Plan, q, k, v, o, d_o, lse, dq, dk, dv, workspac
     _check(st, "zl_coalesced_attn_bwd")
 
 
+def zl_bwd_preprocess(plan: Plan, o, d_o, workspace, stream=None):
+    import torch
+    _check(load_library().zl_bwd_preprocess(
+        plan.handle, _ptr(o, torch.bfloat16, "o", plan.o_elems), _ptr(d_o, torch.bfloat16, "d_o", plan.o_elems),
+        _ptr(workspace, torch.uint8, "workspace", plan.workspace_bytes), _stream(stream)), "zl_bwd_preprocess")
+
+
+def zl_bwd_main(plan: Plan, q, k, v, d_o, lse, dk, dv, workspace, scale: float, stream=None):
+    import torch
+    pq, pk, pv = _qkv(plan, q, k, v)
+    _check(load_library().zl_bwd_main(
+        plan.handle, pq, pk, pv, _ptr(d_o, torch.bfloat16, "d_o", plan.o_elems),
+        _ptr(lse, torch.float32, "lse", plan.lse_elems), _ptr(dk, torch.float32, "dk", plan.dkv_elems),
+        _ptr(dv, torch.float32, "dv", plan.dkv_elems), _ptr(workspace, torch.uint8, "workspace", plan.workspace_bytes),
+        ctypes.c_float(scale), _stream(stream)), "zl_bwd_main")
+
+
+def zl_bwd_finalize(plan: Plan, dq, workspace, scale: float, stream=None):
+    import torch
+    _check(load_library().zl_bwd_finalize(
+        plan.handle, _ptr(dq, torch.float32, "dq", plan.dq_elems),
+        _ptr(workspace, torch.uint8, "workspace", plan.workspace_bytes), ctypes.c_float(scale), _stream(stream)),
+        "zl_bwd_finalize")
+
+
 def zl_get_device_status(plan: Plan, stream=None) -> int:
     s = ctypes.c_int32()
     _check(load_library().zl_get_device_status(plan.handle, _stream(stream), ctypes.byref(s)),
@@ -270,4 +299,5 @@ def exported_symbols() -> List[str]:
     """Names of the entry points declared in include/zl.h."""
     return ["zl_plan_worklist", "zl_plan_destroy", "zl_plan_arena_sizes", "zl_plan_item", "zl_plan_count",
             "zl_plan_tiles", "zl_plan_group", "zl_coalesced_attn_fwd", "zl_merge_partials",
-            "zl_coalesced_attn_bwd", "zl_get_device_status", "zl_status_string", "zl_version"]
+            "zl_coalesced_attn_bwd", "zl_bwd_preprocess", "zl_bwd_main", "zl_bwd_finalize",
+            "zl_get_device_status", "zl_status_string", "zl_version"]

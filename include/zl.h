@@ -93,6 +93,10 @@ typedef struct zl_plan zl_plan;
 /* Flag for zl_plan_worklist: build the host tables only (no device upload).  Such a
  * plan answers the zl_plan_* queries but cannot be launched. */
 #define ZL_PLAN_HOST_ONLY 1u
+/* Test flag (failure detection): the forward launch announces its first K tile but
+ * never issues the copy, so a bounded device wait runs out (after ~20M cycles) and
+ * zl_get_device_status reports ZL_ERR_TIMEOUT; nothing faults or hangs. */
+#define ZL_PLAN_TEST_WITHHOLD_LOAD 2u
 
 /* Validate a work list and build its tile lists (host C++), then upload them to the
  * current device.
@@ -181,6 +185,21 @@ ZL_API zl_status zl_coalesced_attn_bwd(const zl_plan* plan, const void* q, const
                                 const void* v, const void* o, const void* d_o,
                                 const float* lse, float* dq, float* dk, float* dv,
                                 void* workspace, float scale, void* stream);
+
+/* The three launches of zl_coalesced_attn_bwd, callable one by one (same arguments,
+ * same order of use); zl_coalesced_attn_bwd is exactly these three in sequence.
+ *   zl_bwd_preprocess: D_i = rowsum(dO_i * O_i) into the workspace and zeroing of the
+ *     workspace's fp32 dQ accumulator (HBM-bound, one warp per (row, head)).
+ *   zl_bwd_main: the persistent tcgen05 backward over (item, head, 128 KV rows) tiles;
+ *     writes dk, dv and accumulates unscaled dQ in the workspace.
+ *   zl_bwd_finalize: dq = scale * accumulator, per item block. */
+ZL_API zl_status zl_bwd_preprocess(const zl_plan* plan, const void* o, const void* d_o, void* workspace,
+                                   void* stream);
+ZL_API zl_status zl_bwd_main(const zl_plan* plan, const void* q, const void* k, const void* v,
+                             const void* d_o, const float* lse, float* dk, float* dv, void* workspace,
+                             float scale, void* stream);
+ZL_API zl_status zl_bwd_finalize(const zl_plan* plan, float* dq, void* workspace, float scale,
+                                 void* stream);
 
 /* Read and clear the plan's device status word (synchronises `stream`).  *device_status
  * receives ZL_OK or the first error a kernel recorded (ZL_ERR_TIMEOUT when a bounded
