@@ -136,7 +136,7 @@ def dO_arena(plan, work, do_tok, device):
     return arena
 
 
-def cpu_oracle_sample(work, seed=0, rows_per_item=24, heads_per_item=2):
+def cpu_oracle_sample(work, seed=0, rows_per_item=128, heads_per_item=2):
     """Time the oracle (as it stands) on a bounded sample of the workload: for every item,
     `rows_per_item` query rows x `heads_per_item` heads, forward + dQ backward.  Returns
     (TFLOP/s over the sampled algorithmic FLOPs, seconds, description)."""
@@ -205,13 +205,16 @@ def run_gpu(args):
     zl.load_library()
 
     work = config_training()
+    if args.scale > 1:  # smaller case of the same list, for profiler captures
+        from coalesced_packed_attention_gb300.workloads import scaled
+        work = scaled(work, args.scale)
     H, d, T, scale = work.n_heads, work.head_dim, work.total_tokens, work.scale
     F_fwd = work.fwd_flops()
     F_bwd = work.bwd_flops()
     F_step = F_fwd + F_bwd
 
     t_plan = time.perf_counter()
-    plan = zl.zl_plan_worklist(work.items, H, d, T)
+    plan = zl.zl_plan_worklist(work.items, H, d, T, zl.ZL_PLAN_FWD_ONE_SUBTILE if args.fwd_one_subtile else 0)
     t_plan = time.perf_counter() - t_plan
 
     q, k, v, do_tok = make_inputs(T, H, d, seed=rank, with_grad_output=True, device=str(dev))
@@ -364,6 +367,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scale", type=int, default=1,
+                    help="divide every length of the list by this factor (profiler captures only)")
+    ap.add_argument("--fwd-one-subtile", action="store_true",
+                    help="use the 128-row single-warpgroup forward variant")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -81,7 +81,9 @@ extern "C" zl_status zl_coalesced_attn_fwd(const zl_plan* p, const void* q, cons
   fp.o_partial = o_partial;
   fp.lse = lse;
   fp.scale_log2 = scale * 1.44269504088896340736f;
-  cudaError_t e = launch_fwd(p->head_dim, tq, tk, tv, fp, p->num_sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = p->fwd_block == kFwdBlockM
+                      ? launch_fwd2(p->head_dim, tq, tk, tv, fp, p->num_sms, static_cast<cudaStream_t>(stream))
+                      : launch_fwd(p->head_dim, tq, tk, tv, fp, p->num_sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
 

@@ -11,6 +11,7 @@ namespace zl {
 
 constexpr int kBlockM = 128;   // query rows per forward tile / per backward q-step
 constexpr int kBlockN = 128;   // KV rows per forward step / per backward tile
+constexpr int kFwdBlockM = 256;  // query rows per forward tile of the two-sub-tile kernel
 
 // Resolved work item as the kernels read it (device copy of the planner's table).
 struct DevItem {
@@ -55,6 +56,7 @@ struct zl_plan {
   int num_sms = 0;
   bool host_only = false;
   bool test_withhold = false;   // ZL_PLAN_TEST_WITHHOLD_LOAD
+  int32_t fwd_block = zl::kFwdBlockM;  // query rows per forward tile: 256 (two sub-tiles) or 128
 
   std::vector<zl::DevItem> items;
   std::vector<zl_work_item> resolved;

@@ -42,6 +42,9 @@ struct BwdParams {
 cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int num_sms, cudaStream_t stream);
 
+cudaError_t launch_fwd2(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const FwdParams& p, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_merge(int head_dim, const DevGroup* groups, int32_t n_groups, const DevMember* members,
                          int64_t total_rowheads, const float* o_partial, const float* lse_partial,
                          __nv_bfloat16* o, float* lse_out, int num_sms, cudaStream_t stream);

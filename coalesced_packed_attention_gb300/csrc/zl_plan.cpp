@@ -178,9 +178,10 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
   for (int32_t i = 0; i < n; ++i) {
     const DevItem& it = p->items[i];
     const int32_t nqb = (int32_t)ceil_div(it.q_hi - it.q_lo, kBlockM);
+    const int32_t nfb = (int32_t)ceil_div(it.q_hi - it.q_lo, p->fwd_block);
     const int32_t nkb = (int32_t)ceil_div(it.kv_hi - it.kv_lo, kBlockN);
     for (int32_t h = it.h_lo; h < it.h_hi; ++h) {
-      for (int32_t b = 0; b < nqb; ++b) p->fwd_tiles.push_back({i, h, b, nkb});
+      for (int32_t b = 0; b < nfb; ++b) p->fwd_tiles.push_back({i, h, b, nkb});
       for (int32_t b = 0; b < nkb; ++b) p->bwd_tiles.push_back({i, h, b, nqb});
     }
   }
@@ -254,6 +255,7 @@ extern "C" zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items
   p->total_tokens = total_tokens;
   p->host_only = (flags & ZL_PLAN_HOST_ONLY) != 0;
   p->test_withhold = (flags & ZL_PLAN_TEST_WITHHOLD_LOAD) != 0;
+  p->fwd_block = (flags & ZL_PLAN_FWD_ONE_SUBTILE) ? kBlockM : kFwdBlockM;
   zl_status s = build(p, items, n_items);
   if (s == ZL_OK && !p->host_only) s = upload(p);
   if (s != ZL_OK) {

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libzl.so")
 ZL_OK, ZL_ERR_INVALID_ARG, ZL_ERR_ALIGN, ZL_ERR_CUDA, ZL_ERR_TIMEOUT, ZL_ERR_UNSUPPORTED, ZL_ERR_NO_MEMORY = range(7)
 ZL_PLAN_HOST_ONLY = 1
 ZL_PLAN_TEST_WITHHOLD_LOAD = 2
+ZL_PLAN_FWD_ONE_SUBTILE = 4
 
 
 class ZlError(RuntimeError):

@@ -97,12 +97,17 @@ typedef struct zl_plan zl_plan;
  * never issues the copy, so a bounded device wait runs out (after ~20M cycles) and
  * zl_get_device_status reports ZL_ERR_TIMEOUT; nothing faults or hangs. */
 #define ZL_PLAN_TEST_WITHHOLD_LOAD 2u
+/* Forward variant: tiles of 128 query rows with one softmax warpgroup per CTA instead
+ * of the default 256-row tiles split into two 128-row sub-tiles whose softmax
+ * warpgroups alternate on the tensor core.  Both compute the same result. */
+#define ZL_PLAN_FWD_ONE_SUBTILE 4u
 
 /* Validate a work list and build its tile lists (host C++), then upload them to the
  * current device.
  *   items[n_items]: descriptors (host memory, read only; not retained).
  *   n_heads H >= 1, head_dim d in {64, 128}, total_tokens T >= 1 (Q/K/V have T rows).
- * Tiles: forward = (item, head, 128 query rows); backward = (item, head, 128 KV rows).
+ * Tiles: forward = (item, head, 256 query rows; 128 with ZL_PLAN_FWD_ONE_SUBTILE);
+ * backward = (item, head, 128 KV rows).
  * Each list is sorted longest-first (cost = KV blocks for forward, query blocks for
  * backward), ties in work-list order, and a persistent grid of one CTA per SM claims
  * tiles in that order from an atomic counter.

@@ -50,7 +50,7 @@ def sample_rows(n, seed, k=4096):
 class Run:
     """One forward (+ merge, + backward) of a work list on cuda:0."""
 
-    def __init__(self, work, seed=0, structured=False, backward=False, items=None):
+    def __init__(self, work, seed=0, structured=False, backward=False, items=None, flags=0):
         import torch
         ensure_library()
         self.work = work
@@ -59,7 +59,7 @@ class Run:
         self.scale = work.scale
         ins = make_inputs(T, H, d, seed, with_grad_output=backward, structured=structured)
         self.q, self.k, self.v = (x.float().numpy() for x in ins[:3])
-        self.plan = zl.zl_plan_worklist(self.items, H, d, T)
+        self.plan = zl.zl_plan_worklist(self.items, H, d, T, flags)
         dev = torch.device("cuda:0")
         qd, kd, vd = (x.to(dev) for x in ins[:3])
         bufs = zl.allocate(self.plan, dev, backward=backward)

@@ -84,12 +84,12 @@ def test_tiles_cover_every_row_head_once_longest_first(make):
     for (i, h, b, cost) in tiles:
         it = w.items[i]
         assert it.h_lo <= h < it.h_hi
-        assert 0 <= b * 128 < max(it.nq, 1)
+        assert 0 <= b * 256 < max(it.nq, 1)
         assert cost == -(-it.nkv // 128)
         key = (i, h, b)
         assert key not in seen
         seen[key] = 1
-    expected = sum(it.nh * -(-it.nq // 128) for it in w.items)
+    expected = sum(it.nh * -(-it.nq // 256) for it in w.items)
     assert len(tiles) == expected == p.n_fwd_tiles
     costs = [t[3] for t in tiles]
     assert costs == sorted(costs, reverse=True)
