@@ -136,14 +136,19 @@ def dO_arena(plan, work, do_tok, device):
     return arena
 
 
-def cpu_oracle_sample(work, seed=0, rows_per_item=128, heads_per_item=2):
+def oracle_inputs(work, seed=0):
+    from coalesced_packed_attention_gb300.workloads import make_inputs
+    return tuple(x.float().numpy() for x in make_inputs(work.total_tokens, work.n_heads, work.head_dim, seed,
+                                                        with_grad_output=True))
+
+
+def cpu_oracle_sample(work, seed=0, rows_per_item=128, heads_per_item=2, inputs=None):
     """Time the oracle (as it stands) on a bounded sample of the workload: for every item,
     `rows_per_item` query rows x `heads_per_item` heads, forward + dQ backward.  Returns
     (TFLOP/s over the sampled algorithmic FLOPs, seconds, description)."""
     import oracle
-    from coalesced_packed_attention_gb300.workloads import WorkItem, make_inputs
-    q, k, v, do = (x.float().numpy() for x in make_inputs(work.total_tokens, work.n_heads, work.head_dim, seed,
-                                                          with_grad_output=True))
+    from coalesced_packed_attention_gb300.workloads import WorkItem
+    q, k, v, do = inputs if inputs is not None else oracle_inputs(work, seed)
     rng = np.random.default_rng(seed)
     flops = 0
     t0 = time.perf_counter()
@@ -169,11 +174,12 @@ def run_reference(args):
         return
     from coalesced_packed_attention_gb300.workloads import config_training
     work = config_training()
+    inputs = oracle_inputs(work, 0)
     for _ in range(args.warmup):
-        cpu_oracle_sample(work, rows_per_item=4)
+        cpu_oracle_sample(work, rows_per_item=4, inputs=inputs)
     vals, secs = [], []
     for s in range(args.steps):
-        v, dt, desc = cpu_oracle_sample(work, seed=s)
+        v, dt, desc = cpu_oracle_sample(work, seed=s, inputs=inputs)
         vals.append(v)
         secs.append(dt)
     value = float(np.median(vals))

@@ -24,7 +24,8 @@ struct DevItem {
   int64_t dq_offset;       // [|q|,|h|,d] block in dq
   int64_t dkv_offset;      // [|kv|,|h|,d] block in dk and dv
   int64_t ws_d_offset;     // row sums D, [|h|,|q|] floats in the workspace
-  int64_t ws_dq_offset;    // fp32 dQ accumulator, [|q|,|h|,d] floats in the workspace
+  int64_t ws_dq_offset;    // fp32 dQ accumulator, [|q|,|h|,d] floats from the accumulator base
+                           // (which is ws_d_floats floats into the workspace)
   int64_t rowhead_begin;   // prefix of |q|*|h| over items (row-parallel kernels)
 };
 

@@ -171,7 +171,8 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
   p->ws_d_floats = align_up(wsd_next, 4);
   p->ws_dq_floats = wsq_next;
   p->workspace_bytes = 4 * (p->ws_d_floats + p->ws_dq_floats);
-  for (auto& di : p->items) di.ws_dq_offset += p->ws_d_floats;  // dQ accumulators follow D
+  // ws_dq_offset is relative to the dQ accumulator region, which starts ws_d_floats
+  // floats into the workspace (the launchers pass that base pointer)
 
   // ---- tiles, longest first (stable: ties keep work-list, head, block order)
   p->fwd_tiles.clear(); p->bwd_tiles.clear();
@@ -331,5 +332,52 @@ extern "C" zl_status zl_plan_group(const zl_plan* p, int32_t g, int32_t* members
     for (int32_t j = 0; j < G.n_members && j < cap; ++j) members[j] = p->member_items[G.member_begin + j];
   if (out_offset) *out_offset = G.out_offset;
   if (lse_offset) *lse_offset = G.lse_offset;
+  return ZL_OK;
+}
+
+// Host-side dry run of every device access the plan's tables imply: each item's and
+// group's blocks lie inside the arenas zl_plan_arena_sizes reports, and the workspace
+// ranges inside workspace_bytes.  Tile indices address existing items, heads and blocks.
+extern "C" zl_status zl_plan_check_bounds(const zl_plan* p) {
+  if (!p) return ZL_ERR_INVALID_ARG;
+  const int64_t d = p->head_dim;
+  auto in = [](int64_t off, int64_t n, int64_t total) { return n == 0 || (off >= 0 && off + n <= total); };
+  for (size_t i = 0; i < p->items.size(); ++i) {
+    const DevItem& it = p->items[i];
+    const int64_t nq = it.q_hi - it.q_lo, nh = it.h_hi - it.h_lo, nkv = it.kv_hi - it.kv_lo;
+    const int64_t ob = nq * nh * d;
+    if (!in(it.out_offset, ob, it.emit_lse ? p->o_partial_elems : p->o_elems)) return ZL_ERR_INVALID_ARG;
+    if (!in(it.lse_offset, nq * nh, p->lse_elems)) return ZL_ERR_INVALID_ARG;
+    if (!in(it.fin_out_offset, ob, p->o_elems) || !in(it.fin_lse_offset, nq * nh, p->lse_elems))
+      return ZL_ERR_INVALID_ARG;
+    if (!in(it.dq_offset, ob, p->dq_elems) || !in(it.dkv_offset, nkv * nh * d, p->dkv_elems))
+      return ZL_ERR_INVALID_ARG;
+    if (!in(it.ws_d_offset, nq * nh, p->ws_d_floats) || !in(it.ws_dq_offset, ob, p->ws_dq_floats))
+      return ZL_ERR_INVALID_ARG;
+    if (4 * (p->ws_d_floats + p->ws_dq_floats) > p->workspace_bytes) return ZL_ERR_INVALID_ARG;
+  }
+  for (const auto& G : p->groups) {
+    if (!in(G.out_offset, (int64_t)G.nq * G.nh * d, p->o_elems) || !in(G.lse_offset, (int64_t)G.nq * G.nh, p->lse_elems))
+      return ZL_ERR_INVALID_ARG;
+    for (int32_t m = 0; m < G.n_members; ++m) {
+      const DevMember& mb = p->members[G.member_begin + m];
+      if (!in(mb.o_offset, (int64_t)G.nq * G.nh * d, p->o_partial_elems) ||
+          !in(mb.lse_offset, (int64_t)G.nq * G.nh, p->lse_elems))
+        return ZL_ERR_INVALID_ARG;
+    }
+  }
+  const int32_t n = (int32_t)p->items.size();
+  for (const auto& t : p->fwd_tiles) {
+    if (t.item < 0 || t.item >= n) return ZL_ERR_INVALID_ARG;
+    const DevItem& it = p->items[t.item];
+    if (t.head < it.h_lo || t.head >= it.h_hi || (int64_t)t.block * p->fwd_block >= it.q_hi - it.q_lo)
+      return ZL_ERR_INVALID_ARG;
+  }
+  for (const auto& t : p->bwd_tiles) {
+    if (t.item < 0 || t.item >= n) return ZL_ERR_INVALID_ARG;
+    const DevItem& it = p->items[t.item];
+    if (t.head < it.h_lo || t.head >= it.h_hi || (int64_t)t.block * kBlockN >= it.kv_hi - it.kv_lo)
+      return ZL_ERR_INVALID_ARG;
+  }
   return ZL_OK;
 }

@@ -56,6 +56,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "zl_plan_arena_sizes": (I32, [P, pI64, pI64, pI64, pI64, pI64, pI64]),
         "zl_plan_item": (I32, [P, I32, ctypes.POINTER(zl_work_item), pI64, pI64, pI64, pI64, pI32]),
         "zl_plan_count": (I32, [P, I32, pI64]),
+        "zl_plan_check_bounds": (I32, [P]),
         "zl_plan_tiles": (I32, [P, I32, pI32, I64]),
         "zl_plan_group": (I32, [P, I32, pI32, I32, pI32, pI64, pI64]),
         "zl_coalesced_attn_fwd": (I32, [P, P, P, P, P, P, P, F, P]),
@@ -123,6 +124,10 @@ class Plan:
         _check(load_library().zl_plan_item(self.handle, i, ctypes.byref(it), *[ctypes.byref(x) for x in vals],
                                            ctypes.byref(g)), "zl_plan_item")
         return ItemPlacement(it, vals[0].value, vals[1].value, vals[2].value, vals[3].value, g.value)
+
+    def check_bounds(self):
+        """Host dry run: every access a launch would make stays inside the arenas."""
+        _check(load_library().zl_plan_check_bounds(self.handle), "zl_plan_check_bounds")
 
     def tiles(self, which: int = 0):
         """Tile list in scheduler order as a list of (item, head, block, cost)."""
@@ -298,7 +303,8 @@ def backward(plan: Plan, q, k, v, d_o, scale: float, bufs: dict, stream=None) ->
 
 def exported_symbols() -> List[str]:
     """Names of the entry points declared in include/zl.h."""
-    return ["zl_plan_worklist", "zl_plan_destroy", "zl_plan_arena_sizes", "zl_plan_item", "zl_plan_count",
+    return ["zl_plan_worklist", "zl_plan_destroy", "zl_plan_arena_sizes", "zl_plan_item", "zl_plan_check_bounds",
+            "zl_plan_count",
             "zl_plan_tiles", "zl_plan_group", "zl_coalesced_attn_fwd", "zl_merge_partials",
             "zl_coalesced_attn_bwd", "zl_bwd_preprocess", "zl_bwd_main", "zl_bwd_finalize",
             "zl_get_device_status", "zl_status_string", "zl_version"]

@@ -139,6 +139,12 @@ ZL_API zl_status zl_plan_item(const zl_plan* plan, int32_t i, zl_work_item* reso
                        int64_t* fin_out_offset, int64_t* fin_lse_offset, int64_t* dq_offset,
                        int64_t* dkv_offset, int32_t* group);
 
+/* Host-side dry run of the plan: every block and workspace range that a launch with
+ * this plan would touch lies inside the arena sizes of zl_plan_arena_sizes, and every
+ * tile addresses an existing item, head and block.  ZL_OK or ZL_ERR_INVALID_ARG.  Works
+ * on host-only plans (no GPU needed). */
+ZL_API zl_status zl_plan_check_bounds(const zl_plan* plan);
+
 /* Counts: which = 0 forward tiles, 1 backward tiles, 2 merge groups, 3 items. */
 ZL_API zl_status zl_plan_count(const zl_plan* plan, int32_t which, int64_t* count);
 

@@ -156,3 +156,24 @@ def test_flop_counts_of_the_workloads():
     assert abs(config_mixed(with_complement=False).fwd_flops() / 1e12 - 13.39) < 5e-3
     assert abs(config_long_video().fwd_flops() / 1e12 - 269.4) < 0.1
     assert m.bwd_flops() == 5 * m.fwd_flops() // 2
+
+
+def _all_lists():
+    from coalesced_packed_attention_gb300.workloads import Workload, config_training, scaled
+    from tests.gpu_util import tiny_edge_items
+    lists = [config_tiny(), config_images(), config_mixed(), config_long_video(), config_training()]
+    lists += [scaled(w, f) for w in lists[1:] for f in (4, 6, 12, 24)]
+    lists += [Workload("edges", 3, d, 300, tiny_edge_items(3), d ** -0.5) for d in (64, 128)]
+    return lists
+
+
+@pytest.mark.parametrize("flags", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE])
+def test_every_plan_passes_the_bounds_dry_run(flags):
+    for w in _all_lists():
+        p = zl.zl_plan_worklist(w.items, w.n_heads, w.head_dim, w.total_tokens,
+                                flags=zl.ZL_PLAN_HOST_ONLY | flags)
+        p.check_bounds()
+        # the workspace holds D ([|h|,|q|] fp32) and the dQ accumulator ([|q|,|h|,d] fp32)
+        # for every item, and nothing else
+        need = sum(4 * it.nq * it.nh * (1 + w.head_dim) for it in w.items)
+        assert need <= p.workspace_bytes <= need + 16 + 32 * len(w.items)

@@ -36,13 +36,13 @@ def check_backward(r, kv_sample=None, q_sample=None, seed=0):
         do_all = r.do[s + it.q_lo: s + it.q_hi, it.h_lo:it.h_hi]
         rows = np.arange(it.nq) if q_sample is None else sample_rows(it.nq, seed + i, q_sample)
         dQ_ref = oracle.backward_dq(r.q, r.k, r.v, do_all[rows], O[rows], L[:, rows], it, r.scale, it.q_lo + rows)
-        check(f"item{i}.dQ", r.grad(i, "dq")[rows], dQ_ref, ATOL_O)
+        check(f"item{i}.dQ", r.grad(i, "dq")[rows], dQ_ref, ATOL_O, relative=r.relative)
         if it.nkv == 0:
             continue
         kv = np.arange(it.nkv) if kv_sample is None else sample_rows(it.nkv, seed + 7 * i, kv_sample)
         dK_ref, dV_ref = oracle.backward_dkdv(r.q, r.k, r.v, do_all, O, L, it, r.scale, it.kv_lo + kv)
-        check(f"item{i}.dK", r.grad(i, "dk")[kv], dK_ref, ATOL_O)
-        check(f"item{i}.dV", r.grad(i, "dv")[kv], dV_ref, ATOL_O)
+        check(f"item{i}.dK", r.grad(i, "dk")[kv], dK_ref, ATOL_O, relative=r.relative)
+        check(f"item{i}.dV", r.grad(i, "dv")[kv], dV_ref, ATOL_O, relative=r.relative)
 
 
 def test_training_list_scaled_all_rows():
