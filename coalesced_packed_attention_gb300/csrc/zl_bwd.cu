@@ -76,6 +76,21 @@ __device__ __forceinline__ void tensormap_acquire(const void* map) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Fire-and-forget fp32 vector add into global memory (no value returned, so the
+// warpgroup does not wait for the L2 round trip).
+__device__ __forceinline__ void red_add_v4(float* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(__uint_as_float(a)),
+               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+               : "memory");
+}
+
+// Tiles of one (item, head) walk the query blocks starting at different blocks, so
+// CTAs running side by side add into different dQ rows instead of contending on one.
+__device__ __forceinline__ int first_block(int step, int start, int n) {
+  const int b = start + step;
+  return b >= n ? b - n : b;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -183,7 +198,8 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
           tma_load_3d(sV + c * L::kBox, &tm_v, kv_full, 64 * c, tl.head, kvrow);
         }
         const int hl = tl.head - it.h_lo;
-        for (int ib = 0; ib < nqb; ++ib) {
+        for (int is = 0; is < nqb; ++is) {
+          const int ib = first_block(is, tl.block % nqb, nqb);
           const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
           if (!bwait(q_empty + st, ph ^ 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(q_full + st, L::kTile);
@@ -222,7 +238,8 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         if (!bwait(kv_full, kt & 1, abort_flag, p.wait_limit, p.status)) break;
         ++kt;
         tc_fence_after();
-        for (int ib = 0; ib < nqb; ++ib) {
+        for (int is = 0; is < nqb; ++is) {
+          const int ib = first_block(is, tl.block % nqb, nqb);
           const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
           if (!bwait(q_full + st, ph, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
@@ -245,7 +262,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO ; dK += dS^T Q   (K = 128 queries)
-            const uint32_t acc = (ib > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t acc = (is > 0 || kk > 0) ? 1u : 0u;
             mma_ts(tdV, tR0 + kk * 8, sdesc_sw128(aDOs + kk * 2048, L::kBox, 1024), kIdKV, acc);
             mma_ts(tdK, tR0 + 64 + kk * 8, sdesc_sw128(aQs + kk * 2048, L::kBox, 1024), kIdKV, acc);
           }
@@ -293,16 +310,21 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
       float* dq_base = p.ws_dq + it.ws_dq_offset + (int64_t)hl * D;
       bool ok = true;
       float lse_n = kInfB, d_n = 0.f;
-      if (nqb > 0 && t < nq) { lse_n = __ldg(lse_row + t) * kLog2eB; d_n = __ldg(d_row + t); }
-      for (int ib = 0; ib < nqb; ++ib) {
+      const int ib0 = nqb > 0 ? tl.block % nqb : 0;
+      if (nqb > 0 && ib0 * kBlockM + t < nq) {
+        lse_n = __ldg(lse_row + ib0 * kBlockM + t) * kLog2eB;
+        d_n = __ldg(d_row + ib0 * kBlockM + t);
+      }
+      for (int is = 0; is < nqb; ++is) {
+        const int ib = first_block(is, ib0, nqb);
         // publish this block's LSE / D, prefetch the next block's
         sLSE[t] = lse_n;
         sD[t] = d_n;
         mbar_arrive(ld_full);  // bounded stand-in for a warpgroup barrier
         if (!__all_sync(0xffffffffu, bwait(ld_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
-        const int qn = (ib + 1) * kBlockM + t;
+        const int qn = first_block(is + 1, ib0, nqb) * kBlockM + t;
         lse_n = kInfB; d_n = 0.f;
-        if (ib + 1 < nqb && qn < nq) { lse_n = __ldg(lse_row + qn) * kLog2eB; d_n = __ldg(d_row + qn); }
+        if (is + 1 < nqb && qn < nq) { lse_n = __ldg(lse_row + qn) * kLog2eB; d_n = __ldg(d_row + qn); }
 
         if (!__all_sync(0xffffffffu, bwait(sp_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
@@ -362,9 +384,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
           if (q_local < nq) {
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
-              atomicAdd(reinterpret_cast<float4*>(dst + 32 * c + 4 * v4),
-                        make_float4(__uint_as_float(u[4 * v4]), __uint_as_float(u[4 * v4 + 1]),
-                                    __uint_as_float(u[4 * v4 + 2]), __uint_as_float(u[4 * v4 + 3])));
+              red_add_v4(dst + 32 * c + 4 * v4, u[4 * v4], u[4 * v4 + 1], u[4 * v4 + 2], u[4 * v4 + 3]);
           }
         }
         tc_fence_before();

@@ -302,23 +302,28 @@ __global__ void __launch_bounds__(320, 1)
           for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(u[e]);
         }
         const int valid = nkv - j * kBlockN;
-        float mx = kNegInfv;
-        if (valid >= kBlockN) {
+        if (valid < kBlockN) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) {
+          for (int c = 0; c < 128; ++c)
             if (c >= valid) s[c] = kNegInfv;
-            mx = fmaxf(mx, s[c]);
-          }
         }
+        // row max as 8 independent chains (one warp per sub-partition per warpgroup
+        // leaves little room to hide a 128-long dependent chain)
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(s[e], s[e + 8]);
+#pragma unroll
+        for (int c = 16; c < 128; c += 8)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[c + e]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_blk = mx * sl2;
         const bool need = m_blk > m_used + kThr;
         const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
         const float f = need ? ex2(m_used - m_blk) : 1.f;  // exp2(-inf) = 0 on the first block
         if (need) { l *= f; m_used = m_blk; }
-        float sum = 0.f;
+        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -326,12 +331,13 @@ __global__ void __launch_bounds__(320, 1)
           for (int e = 0; e < 16; ++e) {
             const float p0 = ex2(fmaf(s[32 * c + 2 * e], sl2, -m_used));
             const float p1 = ex2(fmaf(s[32 * c + 2 * e + 1], sl2, -m_used));
-            sum += p0 + p1;
+            sum8[(2 * e) & 7] += p0;
+            sum8[(2 * e + 1) & 7] += p1;
             pk[e] = pack_bf16(p0, p1);
           }
           tmem_st16(tS + 16 * c, pk);
         }
-        l += sum;
+        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         if (rescale) {
           // S_w,j was issued after PV_w,{j-1}: its commit proves O_w stable here, and
           // PV_w,j waits for this warpgroup's P handoff below

@@ -13,6 +13,11 @@ from tests._lib import ensure_library
 # accumulation), plus a normwise co-gate ||err||_F / ||ref||_F <= 2e-2 so that a long
 # sequence, where |O| ~ 1/sqrt(L) is below the absolute gate, cannot pass with O = 0.
 ATOL_O, ATOL_LSE, RTOL_F = 1e-2, 1e-3, 2e-2
+# Structured inputs (Q x 4, V + 3): gradients are gated at 2.5% of max|ref|.  The row
+# sums D_i = dO_i . O_i are formed from the stored bf16 O, whose rounding (2^-9 |O|,
+# with |O| ~ 3 here) moves D by ~2^-9 * 3 * sqrt(d) and dS = P (dP - D) with it; with
+# N(0,1) inputs the same effect stays far below the 1e-2 absolute gate.
+ATOL_GRAD_STRUCTURED = 2.5e-2
 
 
 def check(name, got, ref, atol, rtol_f=RTOL_F, relative=False):
