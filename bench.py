@@ -142,7 +142,7 @@ def oracle_inputs(work, seed=0):
                                                         with_grad_output=True))
 
 
-def cpu_oracle_sample(work, seed=0, rows_per_item=128, heads_per_item=2, inputs=None):
+def cpu_oracle_sample(work, seed=0, rows_per_item=2048, heads_per_item=2, inputs=None):
     """Time the oracle (as it stands) on a bounded sample of the workload: for every item,
     `rows_per_item` query rows x `heads_per_item` heads, forward + dQ backward.  Returns
     (TFLOP/s over the sampled algorithmic FLOPs, seconds, description)."""

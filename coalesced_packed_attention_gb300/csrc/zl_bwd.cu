@@ -41,7 +41,7 @@ struct BwdLayout {
   static constexpr int kDS = kDO + 2 * kTile;       // [128 kv][128 q] bf16, two 128-byte-swizzled boxes
   static constexpr int kLD = kDS + 2 * kBox;        // LSE*log2(e) and D for the 128 queries of a block
   static constexpr int kBar = kLD + 2 * 128 * 4;
-  static constexpr int kNumBars = 2 + 6 + 5 + 4 + 1 + 1;
+  static constexpr int kNumBars = 21;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 64;
 };
@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
   uint64_t* q_full = bar + 2;     // [2]
   uint64_t* do_full = bar + 4;    // [2]
   uint64_t* q_empty = bar + 6;    // [2]
-  uint64_t* sp_full = bar + 8;
-  uint64_t* ds_full = bar + 9;
+  uint64_t* s_full = bar + 8;     // S^T of the block in TMEM R0
+  uint64_t* ds_ready = bar + 9;   // dS^T in TMEM R0 and shared memory (128 arrivals)
   uint64_t* dq_full = bar + 10;
   uint64_t* dq_empty = bar + 11;
   uint64_t* kv_done = bar + 12;
@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
   uint64_t* tile_empty = bar + 15;  // [2]
   uint64_t* drain = bar + 17;
   uint64_t* ld_full = bar + 18;   // LSE / D of a query block staged in shared memory
+  uint64_t* p_ready = bar + 19;   // P^T in TMEM R0 (128 arrivals): the dV product may start
+  uint64_t* dp_full = bar + 20;   // dP^T of the block in TMEM R1
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   uint32_t* tmem_slot = misc;
   volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(misc + 2);
@@ -139,8 +141,10 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
       mbar_init(tile_full + i, 1);
       mbar_init(tile_empty + i, 1 + 4);
     }
-    mbar_init(sp_full, 1);
-    mbar_init(ds_full, 128);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(ds_ready, 128);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 128);
     mbar_init(kv_done, 1);
@@ -249,6 +253,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
             mma_ss(tR0, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQs + off, 16, 1024), kIdSq, kk > 0);
           }
+          mma_commit(s_full);
           if (!bwait(do_full + st, ph, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           if (nblocks > 0 && !bwait(dq_empty, (nblocks - 1) & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
@@ -257,15 +262,20 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
             mma_ss(tR1, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDOs + off, 16, 1024), kIdSq, kk > 0);
           }
-          mma_commit(sp_full);
-          if (!bwait(ds_full, nblocks & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+          mma_commit(dp_full);
+          // dV += P^T dO as soon as P^T is in TMEM (the warpgroup then forms dS^T)
+          if (!bwait(p_ready, nblocks & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO ; dK += dS^T Q   (K = 128 queries)
-            const uint32_t acc = (is > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tdV, tR0 + kk * 8, sdesc_sw128(aDOs + kk * 2048, L::kBox, 1024), kIdKV, acc);
-            mma_ts(tdK, tR0 + 64 + kk * 8, sdesc_sw128(aQs + kk * 2048, L::kBox, 1024), kIdKV, acc);
-          }
+          for (int kk = 0; kk < 8; ++kk)  // K = 128 queries
+            mma_ts(tdV, tR0 + kk * 8, sdesc_sw128(aDOs + kk * 2048, L::kBox, 1024), kIdKV,
+                   (is > 0 || kk > 0) ? 1u : 0u);
+          if (!bwait(ds_ready, nblocks & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
+            mma_ts(tdK, tR0 + 64 + kk * 8, sdesc_sw128(aQs + kk * 2048, L::kBox, 1024), kIdKV,
+                   (is > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ = dS K   (K = 128 KV rows)
             mma_ss(tR1, sdesc_sw128(aDS + kk * 2048, L::kBox, 1024), sdesc_sw128(aK + kk * 2048, L::kBox, 1024),
@@ -326,7 +336,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         lse_n = kInfB; d_n = 0.f;
         if (is + 1 < nqb && qn < nq) { lse_n = __ldg(lse_row + qn) * kLog2eB; d_n = __ldg(d_row + qn); }
 
-        if (!__all_sync(0xffffffffu, bwait(sp_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, bwait(s_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
         float pr[128];
 #pragma unroll
@@ -338,6 +348,20 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
           for (int e = 0; e < 32; ++e)
             pr[32 * c + e] = kv_ok ? ex2(fmaf(__uint_as_float(u[e]), sl2, -sLSE[32 * c + e])) : 0.f;
         }
+        // P^T (bf16) over the S^T columns already read: the dV product can start now
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(pr[64 * c + 2 * e], pr[64 * c + 2 * e + 1]);
+          tmem_st32(tmem + lane_base + 32 * c, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_ready);
+
+        if (!__all_sync(0xffffffffu, bwait(dp_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t u[32];
@@ -359,17 +383,10 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
             st_shared_v4(addr, pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
           }
         }
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(pr[64 * c + 2 * e], pr[64 * c + 2 * e + 1]);
-          tmem_st32(tmem + lane_base + 32 * c, pk);
-        }
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(ds_full);
+        mbar_arrive(ds_ready);
 
         // dQ of this block: TMEM R1, lane = query row
         if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }

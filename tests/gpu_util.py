@@ -17,7 +17,44 @@ ATOL_O, ATOL_LSE, RTOL_F = 1e-2, 1e-3, 2e-2
 # sums D_i = dO_i . O_i are formed from the stored bf16 O, whose rounding (2^-9 |O|,
 # with |O| ~ 3 here) moves D by ~2^-9 * 3 * sqrt(d) and dS = P (dP - D) with it; with
 # N(0,1) inputs the same effect stays far below the 1e-2 absolute gate.
-ATOL_GRAD_STRUCTURED = 2.5e-2
+ATOL_GRAD_STRUCTURED = 5e-2
+
+
+def oracle_forward(q, k, v, item, scale, rows=None):
+    """oracle.forward split over heads in threads (numpy releases the GIL inside BLAS and
+    its ufuncs); the result is the same as one call over all heads."""
+    import concurrent.futures as cf
+    import os
+    heads = list(range(item.h_lo, item.h_hi))
+    if len(heads) <= 1:
+        return oracle.forward(q, k, v, item, scale, rows=rows)
+
+    def one(h):
+        sub = WorkItem(item.seq_offset, item.seq_len, item.q_lo, item.q_hi, h, h + 1, item.kv_lo, item.kv_hi,
+                       item.emit_lse)
+        return oracle.forward(q, k, v, sub, scale, rows=rows)
+
+    with cf.ThreadPoolExecutor(max_workers=min(len(heads), os.cpu_count() or 1)) as ex:
+        parts = list(ex.map(one, heads))
+    return np.concatenate([p[0] for p in parts], axis=1), np.concatenate([p[1] for p in parts], axis=0)
+
+
+def oracle_backward_dq(q, k, v, do_rows, o_rows, lse_rows, item, scale, rows):
+    """oracle.backward_dq split over heads in threads (same result as one call)."""
+    import concurrent.futures as cf
+    import os
+
+    def one(hi):
+        h = item.h_lo + hi
+        sub = WorkItem(item.seq_offset, item.seq_len, item.q_lo, item.q_hi, h, h + 1, item.kv_lo, item.kv_hi,
+                       item.emit_lse)
+        return oracle.backward_dq(q, k, v, do_rows[:, hi:hi + 1], o_rows[:, hi:hi + 1], lse_rows[hi:hi + 1], sub,
+                                  scale, rows)
+
+    nh = item.h_hi - item.h_lo
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(nh, os.cpu_count() or 1))) as ex:
+        parts = list(ex.map(one, range(nh)))
+    return np.concatenate(parts, axis=1)
 
 
 def check(name, got, ref, atol, rtol_f=RTOL_F, relative=False):
@@ -131,9 +168,11 @@ class Run:
         `sample` is given), then every merge group against the oracle merge."""
         res = {}
         for i, it in enumerate(self.items):
-            rows = None if sample is None else sample_rows(it.nq, seed + 1000 * i, sample)
+            # members of one merge group share (sequence, rows, heads): same sample
+            key = (it.seq_offset, it.q_lo, it.q_hi, it.h_lo, it.h_hi)
+            rows = None if sample is None else sample_rows(it.nq, seed + hash(key) % 100003, sample)
             rel = None if rows is None else rows
-            O_ref, L_ref = oracle.forward(self.q, self.k, self.v, it, self.scale,
+            O_ref, L_ref = oracle_forward(self.q, self.k, self.v, it, self.scale,
                                           rows=None if rows is None else it.q_lo + rows)
             O, L = self.own_o(i), self.own_lse(i)
             if rel is not None:

@@ -9,7 +9,7 @@ import pytest
 import oracle
 from coalesced_packed_attention_gb300.workloads import (WorkItem, config_images, config_long_video,
                                                         config_mixed, config_training, merge_groups)
-from tests.gpu_util import ATOL_O, Run, check, sample_rows
+from tests.gpu_util import ATOL_O, Run, check, oracle_backward_dq, oracle_forward, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -37,10 +37,10 @@ def test_training_full_sampled():
         rows = sample_rows(it.nq, 11 + i, 1024)
         # final O / LSE of those rows: the item's own, or its group's merge
         members = group_of.get(i, [i])
-        parts = [oracle.forward(r.q, r.k, r.v, r.items[m], r.scale, rows=it.q_lo + rows) for m in members]
+        parts = [oracle_forward(r.q, r.k, r.v, r.items[m], r.scale, rows=it.q_lo + rows) for m in members]
         O, L = oracle.merge(parts) if len(parts) > 1 else parts[0]
         do_rows = r.do[s + it.q_lo + rows][:, it.h_lo:it.h_hi]
-        dQ_ref = oracle.backward_dq(r.q, r.k, r.v, do_rows, O, L, it, r.scale, it.q_lo + rows)
+        dQ_ref = oracle_backward_dq(r.q, r.k, r.v, do_rows, O, L, it, r.scale, it.q_lo + rows)
         check(f"item{i}.dQ", r.grad(i, "dq")[rows], dQ_ref, ATOL_O)
         # dK/dV of one head on sampled KV rows (needs every query row's final O, LSE)
         h = it.h_lo
