@@ -212,6 +212,30 @@ ZL_API zl_status zl_bwd_main(const zl_plan* plan, const void* q, const void* k, 
 ZL_API zl_status zl_bwd_finalize(const zl_plan* plan, float* dq, void* workspace, float scale,
                                  void* stream);
 
+/* Forward launch that allocates no device memory (no counterpart in the paper; it
+ * serves callers that cannot call cudaMalloc, e.g. code whose host framework owns all
+ * device memory through its own pool, or an embedding that forbids device allocation
+ * after start-up, and so cannot create a zl_plan, which uploads its tables to memory
+ * the library allocates).
+ *   Arguments: the work list and sizes as for zl_plan_worklist, then the buffers and
+ *   scale as for zl_coalesced_attn_fwd.  Output placement is exactly the planner's
+ *   default, so outputs land where a plan built from the same list would put them (ask
+ *   a host-only plan, ZL_PLAN_HOST_ONLY, for the offsets and arena sizes).
+ *   Scratch: the item table, tile list, scheduler counter and status word live in a
+ *   fixed 8 MiB array compiled into the library; every GPU that loads the library holds
+ *   it until the process exits.  A list whose tables do not fit (about 500 000 tiles of
+ *   256 query rows) is rejected with ZL_ERR_INVALID_ARG before any device work.
+ *   The first call on a device looks up that array's device address (once per device,
+ *   with the device current); make that first call before any stream capture.
+ *   Every call shares the array and zeroes the counter and status word itself, so calls
+ *   whose launches overlap on the GPU (different streams, different threads) race on
+ *   it: order them.  The device status word is not reported by this entry point.
+ *   Calls no cudaMalloc/cudaFree or other allocating routine. */
+ZL_API zl_status zl_coalesced_attn_fwd_noalloc(const zl_work_item* items, int32_t n_items, int32_t n_heads,
+                                               int32_t head_dim, int64_t total_tokens, const void* q,
+                                               const void* k, const void* v, void* o, float* o_partial,
+                                               float* lse, float scale, void* stream);
+
 /* Read and clear the plan's device status word (synchronises `stream`).  *device_status
  * receives ZL_OK or the first error a kernel recorded (ZL_ERR_TIMEOUT when a bounded
  * wait gave up; the kernel then stopped cleanly instead of hanging). */

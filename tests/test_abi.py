@@ -30,7 +30,9 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert sorted(zl.exported_symbols()) == sorted(n for n in names if n in zl.exported_symbols())
-    assert set(names) <= set(zl.exported_symbols()) | set(getattr(zl, "EXTRA_SYMBOLS", []))
+    # every declared entry point has a Python binding, except the allocation-free
+    # forward, whose callers (and its test) use the C ABI directly
+    assert set(names) - {"zl_coalesced_attn_fwd_noalloc"} <= set(zl.exported_symbols())
 
 
 def test_status_strings(lib):
