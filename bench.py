@@ -365,6 +365,59 @@ def run_gpu(args):
         torch.distributed.destroy_process_group()
 
 
+def run_additivity(args):
+    """Co-location check of the additive time model: every work item timed alone (a plan
+    holding only that item, same inputs) against the coalesced launch of the whole list,
+    forward + merge + backward.  The pages' profiler prices each (bucket, configuration)
+    pair separately and takes a rank's time as their sum, assuming that co-locating whole
+    sequences with shards costs nothing extra (pith.science review, "Load-bearing premise").
+    ratio = coalesced / sum of solo times: 1.0 means additive, < 1 means co-location helps
+    (the persistent launch fills SMs that a lone item would leave idle)."""
+    import torch
+    from coalesced_packed_attention_gb300 import zl
+    from coalesced_packed_attention_gb300.workloads import config_training, make_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    work = config_training()
+    if args.scale > 1:
+        from coalesced_packed_attention_gb300.workloads import scaled
+        work = scaled(work, args.scale)
+    H, d, T, scale = work.n_heads, work.head_dim, work.total_tokens, work.scale
+    q, k, v, do_tok = make_inputs(T, H, d, seed=0, with_grad_output=True, device=str(dev))
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(items, reps):
+        plan = zl.zl_plan_worklist(items, H, d, T)
+        d_o = dO_arena(plan, type(work)(work.name, H, d, T, list(items), scale), do_tok, dev)
+        bufs = zl.allocate(plan, dev, backward=True)
+
+        def step():
+            zl.zl_coalesced_attn_fwd(plan, q, k, v, bufs["o"], bufs["o_partial"], bufs["lse"], scale, stream)
+            zl.zl_merge_partials(plan, bufs["o_partial"], bufs["lse"], bufs["o"], bufs["lse"], stream)
+            zl.zl_coalesced_attn_bwd(plan, q, k, v, bufs["o"], d_o, bufs["lse"], bufs["dq"], bufs["dk"], bufs["dv"],
+                                     bufs["workspace"], scale, stream)
+        for _ in range(2):
+            step()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(reps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    coalesced = timed(work.items, args.steps)
+    solo = [timed([it], max(1, args.steps // 2)) for it in work.items]
+    line = {"additivity": {
+        "workload": work.name, "coalesced_ms": coalesced, "sum_solo_ms": float(sum(solo)),
+        "ratio": coalesced / float(sum(solo)),
+        "items": [{"label": lab, "solo_ms": s, "fwd_tflop": it.fwd_flops(d) / 1e12}
+                  for lab, s, it in zip(work.labels, solo, work.items)]}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -377,8 +430,12 @@ def main():
                     help="divide every length of the list by this factor (profiler captures only)")
     ap.add_argument("--fwd-one-subtile", action="store_true",
                     help="use the 128-row single-warpgroup forward variant")
+    ap.add_argument("--additivity", action="store_true",
+                    help="time every work item alone and the coalesced list (co-location check)")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.additivity:
+        run_additivity(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -76,13 +76,20 @@ __device__ __forceinline__ void tensormap_acquire(const void* map) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Fire-and-forget fp32 vector add into global memory (no value returned, so the
-// warpgroup does not wait for the L2 round trip).
-__device__ __forceinline__ void red_add_v4(float* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(__uint_as_float(a)),
-               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
-               : "memory");
+// TMA tensor reduce-add (fp32 add into global memory) of one shared-memory box, issued
+// by one thread and tracked by its bulk-async group.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* map, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
 }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The shared-memory sources of this thread's bulk groups have been read.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// This thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Tiles of one (item, head) walk the query blocks starting at different blocks, so
 // CTAs running side by side add into different dQ rows instead of contending on one.
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         const int nq = it.q_hi - it.q_lo;
         const int nqb = (nq + kBlockM - 1) / kBlockM;
         if (nqb == 0) continue;
-        const CUtensorMap* tm_do = p.do_maps + tl.item;
+        const CUtensorMap* tm_do = p.do_maps + 2 * tl.item;
         tensormap_acquire(tm_do);
         if (!bwait(kv_empty, (kt & 1) ^ 1, abort_flag, p.wait_limit, p.status)) break;
         ++kt;
@@ -317,7 +324,8 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
       const bool kv_ok = kv_local < nkv;
       const float* lse_row = p.lse + it.fin_lse_offset + (int64_t)hl * nq;
       const float* d_row = p.ws_d + it.ws_d_offset + (int64_t)hl * nq;
-      float* dq_base = p.ws_dq + it.ws_dq_offset + (int64_t)hl * D;
+      const CUtensorMap* tm_dq = p.do_maps + 2 * tl.item + 1;  // this item's dQ accumulator
+      if (lane == 0) tensormap_acquire(tm_dq);
       bool ok = true;
       float lse_n = kInfB, d_n = 0.f;
       const int ib0 = nqb > 0 ? tl.block % nqb : 0;
@@ -361,6 +369,10 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         mbar_arrive(p_ready);
 
         if (!__all_sync(0xffffffffu, bwait(dp_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
+        // this warp's rows of the dS^T buffer held the previous block's dQ boxes: the TMA
+        // must have read them before they are overwritten
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -388,24 +400,41 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         tc_fence_before();
         mbar_arrive(ds_ready);
 
-        // dQ of this block: TMEM R1, lane = query row
+        // dQ of this block (TMEM R1, lane = query row) into the fp32 accumulator: each warp
+        // stages its 32 rows in the dS^T buffer (free once the dQ product is done) as
+        // 128-byte-swizzled boxes of 32 rows x 32 floats and adds them with TMA tensor
+        // reduce-adds (one instruction per box, rows past the item clipped by the map)
         if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
-        const int q_local = ib * kBlockM + t;
-        float* dst = dq_base + (int64_t)q_local * nh * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_base + 128 + 32 * c, u);
+        for (int half = 0; half < D / 64; ++half) {
+          uint32_t u0[32], u1[32];
+          tmem_ld32(tmem + lane_base + 128 + 64 * half, u0);
+          tmem_ld32(tmem + lane_base + 128 + 64 * half + 32, u1);
           tmem_ld_wait();
-          if (q_local < nq) {
+          if (half == D / 64 - 1) {  // R1 fully read: the next block's dP^T may overwrite it
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+          }
+          if (half > 0) {  // the previous half's boxes must have been read by the TMA
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+          }
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              red_add_v4(dst + 32 * c + 4 * v4, u[4 * v4], u[4 * v4 + 1], u[4 * v4 + 2], u[4 * v4 + 3]);
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t off = (uint32_t)((j ^ (t & 7)) << 4);
+            st_shared_v4(aDSrow + off, u0[4 * j], u0[4 * j + 1], u0[4 * j + 2], u0[4 * j + 3]);
+            st_shared_v4(aDSrow + L::kBox + off, u1[4 * j], u1[4 * j + 1], u1[4 * j + 2], u1[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int row = ib * kBlockM + (warp & 3) * 32;
+            tma_reduce_add_3d(tm_dq, sDS + (warp & 3) * 4096, 64 * half, hl, row);
+            tma_reduce_add_3d(tm_dq, sDS + L::kBox + (warp & 3) * 4096, 64 * half + 32, hl, row);
+            bulk_commit();
           }
         }
-        tc_fence_before();
-        mbar_arrive(dq_empty);
         ++nblocks;
       }
       if (!ok) break;
@@ -441,6 +470,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
       }
       tc_fence_before();
     }
+    if (lane == 0) bulk_wait0();  // every dQ reduce-add of this warp has completed
   }
 
   tc_fence_before();

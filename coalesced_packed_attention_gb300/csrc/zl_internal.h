@@ -79,6 +79,7 @@ struct zl_plan {
   zl::DevGroup* d_groups = nullptr;
   zl::DevMember* d_members = nullptr;
   int32_t* d_counters = nullptr;
-  CUtensorMap* d_do_maps = nullptr;          // per item, rewritten by every backward call
+  CUtensorMap* d_do_maps = nullptr;          // 2 per item (dO block, dQ accumulator block),
+                                             // rewritten by every backward call
   std::vector<CUtensorMap> h_do_maps;        // host staging of the same
 };

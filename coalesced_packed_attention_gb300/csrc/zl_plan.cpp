@@ -215,7 +215,7 @@ zl_status upload(zl_plan* p) {
                        align_up(sizeof(DevGroup) * p->groups.size(), 256) +
                        align_up(sizeof(DevMember) * p->members.size(), 256) +
                        align_up(sizeof(int32_t) * kNumCounters, 256) +
-                       align_up(sizeof(CUtensorMap) * p->items.size(), 256);
+                       align_up(sizeof(CUtensorMap) * 2 * p->items.size(), 256);
   if (cudaMalloc(&p->dev_blob, bytes) != cudaSuccess) { p->dev_blob = nullptr; return ZL_ERR_NO_MEMORY; }
   char* cur = static_cast<char*>(p->dev_blob);
   p->d_items = carve<DevItem>(cur, p->items.size());
@@ -224,8 +224,8 @@ zl_status upload(zl_plan* p) {
   p->d_groups = carve<DevGroup>(cur, p->groups.size());
   p->d_members = carve<DevMember>(cur, p->members.size());
   p->d_counters = carve<int32_t>(cur, kNumCounters);
-  p->d_do_maps = carve<CUtensorMap>(cur, p->items.size());
-  p->h_do_maps.resize(p->items.size());
+  p->d_do_maps = carve<CUtensorMap>(cur, 2 * p->items.size());
+  p->h_do_maps.resize(2 * p->items.size());
   auto cp = [](void* dst, const void* src, size_t n) {
     return n == 0 || cudaMemcpy(dst, src, n, cudaMemcpyHostToDevice) == cudaSuccess;
   };
