@@ -98,12 +98,17 @@ __device__ __forceinline__ int first_block(int step, int start, int n) {
   return b >= n ? b - n : b;
 }
 
+// TMEM column of the packed bf16 P^T for MMA K-step kk (16 queries): queries 0-63 are
+// packed by warpgroup 0 into R0 columns [0,32), queries 64-127 by warpgroup 1 into
+// [64,96); the dS^T halves sit 32 columns further on.
+__device__ __forceinline__ uint32_t pcol(int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); }
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                         const __grid_constant__ CUtensorMap tm_k,
                                                         const __grid_constant__ CUtensorMap tm_v,
                                                         const BwdParams p) {
@@ -146,26 +151,26 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
       mbar_init(do_full + i, 1);
       mbar_init(q_empty + i, 1);
       mbar_init(tile_full + i, 1);
-      mbar_init(tile_empty + i, 1 + 4);
+      mbar_init(tile_empty + i, 1 + 8);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_ready, 128);
-    mbar_init(ds_ready, 128);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(dq_empty, 256);
     mbar_init(kv_done, 1);
     mbar_init(drain, 1);
-    mbar_init(ld_full, 128);
+    mbar_init(ld_full, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -179,7 +184,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
   uint8_t* sDO = smem + L::kDO;
   uint8_t* sDS = smem + L::kDS;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t tile_it = 0, kt = 0, qit = 0;
@@ -224,7 +229,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdSq = idesc_bf16(128, 128, false, false);
@@ -275,13 +280,13 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // K = 128 queries
-            mma_ts(tdV, tR0 + kk * 8, sdesc_sw128(aDOs + kk * 2048, L::kBox, 1024), kIdKV,
+            mma_ts(tdV, tR0 + pcol(kk), sdesc_sw128(aDOs + kk * 2048, L::kBox, 1024), kIdKV,
                    (is > 0 || kk > 0) ? 1u : 0u);
           if (!bwait(ds_ready, nblocks & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
-            mma_ts(tdK, tR0 + 64 + kk * 8, sdesc_sw128(aQs + kk * 2048, L::kBox, 1024), kIdKV,
+            mma_ts(tdK, tR0 + 32 + pcol(kk), sdesc_sw128(aQs + kk * 2048, L::kBox, 1024), kIdKV,
                    (is > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ = dS K   (K = 128 KV rows)
@@ -300,11 +305,18 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
       bwait(drain, 0, abort_flag, p.wait_limit, p.status);
     }
   } else {
-    // ------------------------------------------------------------ softmax / dQ warpgroup
-    const int t = threadIdx.x;  // KV row of the tile for P/dS, query row of the block for dQ
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax / dQ warpgroups
+    // Two warpgroups share the TMEM lanes (lane = KV row for P/dS, query row for dQ) and
+    // split the columns: warpgroup wg takes queries [64wg, 64wg+64) of S^T and dP^T and
+    // head-dim columns [wg d/2, (wg+1) d/2) of dQ, dK and dV.
+    constexpr int kHalfD = D / 2;
+    const int wg = warp >> 2;
+    const int t = threadIdx.x & 127;  // KV row of the tile for P/dS, query row of the block for dQ
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int qc0 = 64 * wg;          // this warpgroup's query columns
+    const int dc0 = kHalfD * wg;      // this warpgroup's head-dim columns
     const float sl2 = p.scale_log2;
-    const uint32_t aDSrow = smem_u32(sDS) + t * 128;
+    const uint32_t aDSrow = smem_u32(sDS) + wg * L::kBox + t * 128;  // row t of box wg
     uint32_t tile_it = 0, nblocks = 0, ntiles = 0;
     for (;;) {
       const uint32_t slot = tile_it & 1;
@@ -327,72 +339,76 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
       const CUtensorMap* tm_dq = p.do_maps + 2 * tl.item + 1;  // this item's dQ accumulator
       if (lane == 0) tensormap_acquire(tm_dq);
       bool ok = true;
-      float lse_n = kInfB, d_n = 0.f;
+      float lse_n = kInfB, d_n = 0.f;  // warpgroup 0 stages LSE / D of query t of each block
       const int ib0 = nqb > 0 ? tl.block % nqb : 0;
-      if (nqb > 0 && ib0 * kBlockM + t < nq) {
+      if (wg == 0 && nqb > 0 && ib0 * kBlockM + t < nq) {
         lse_n = __ldg(lse_row + ib0 * kBlockM + t) * kLog2eB;
         d_n = __ldg(d_row + ib0 * kBlockM + t);
       }
       for (int is = 0; is < nqb; ++is) {
         const int ib = first_block(is, ib0, nqb);
         // publish this block's LSE / D, prefetch the next block's
-        sLSE[t] = lse_n;
-        sD[t] = d_n;
-        mbar_arrive(ld_full);  // bounded stand-in for a warpgroup barrier
+        if (wg == 0) {
+          sLSE[t] = lse_n;
+          sD[t] = d_n;
+        }
+        mbar_arrive(ld_full);  // bounded stand-in for a barrier of both warpgroups
         if (!__all_sync(0xffffffffu, bwait(ld_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
-        const int qn = first_block(is + 1, ib0, nqb) * kBlockM + t;
-        lse_n = kInfB; d_n = 0.f;
-        if (is + 1 < nqb && qn < nq) { lse_n = __ldg(lse_row + qn) * kLog2eB; d_n = __ldg(d_row + qn); }
+        if (wg == 0) {
+          const int qn = first_block(is + 1, ib0, nqb) * kBlockM + t;
+          lse_n = kInfB; d_n = 0.f;
+          if (is + 1 < nqb && qn < nq) { lse_n = __ldg(lse_row + qn) * kLog2eB; d_n = __ldg(d_row + qn); }
+        }
 
         if (!__all_sync(0xffffffffu, bwait(s_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
-        float pr[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_base + 32 * c, u);
+        float pr[64];
+        {
+          uint32_t u0[32], u1[32];
+          tmem_ld32(tmem + lane_base + qc0, u0);
+          tmem_ld32(tmem + lane_base + qc0 + 32, u1);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            pr[32 * c + e] = kv_ok ? ex2(fmaf(__uint_as_float(u[e]), sl2, -sLSE[32 * c + e])) : 0.f;
+          for (int e = 0; e < 32; ++e) {
+            pr[e] = kv_ok ? ex2(fmaf(__uint_as_float(u0[e]), sl2, -sLSE[qc0 + e])) : 0.f;
+            pr[32 + e] = kv_ok ? ex2(fmaf(__uint_as_float(u1[e]), sl2, -sLSE[qc0 + 32 + e])) : 0.f;
+          }
         }
-        // P^T (bf16) over the S^T columns already read: the dV product can start now
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        // P^T (bf16) over this warpgroup's S^T columns, already read: dV may start now
+        {
           uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(pr[64 * c + 2 * e], pr[64 * c + 2 * e + 1]);
-          tmem_st32(tmem + lane_base + 32 * c, pk);
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(pr[2 * e], pr[2 * e + 1]);
+          tmem_st32(tmem + lane_base + qc0, pk);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_ready);
 
         if (!__all_sync(0xffffffffu, bwait(dp_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
-        // this warp's rows of the dS^T buffer held the previous block's dQ boxes: the TMA
-        // must have read them before they are overwritten
+        // this warp's rows of box wg held the previous block's dQ boxes: the TMA must
+        // have read them before they are overwritten
         if (lane == 0) bulk_wait_read0();
         __syncwarp();
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t u[32];
-          tmem_ld32(tmem + lane_base + 128 + 32 * c, u);
+          tmem_ld32(tmem + lane_base + 128 + qc0 + 32 * c, u);
           tmem_ld_wait();
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float a = pr[32 * c + 2 * e] * (__uint_as_float(u[2 * e]) - sD[32 * c + 2 * e]);
-            const float b2 = pr[32 * c + 2 * e + 1] * (__uint_as_float(u[2 * e + 1]) - sD[32 * c + 2 * e + 1]);
+            const float a = pr[32 * c + 2 * e] * (__uint_as_float(u[2 * e]) - sD[qc0 + 32 * c + 2 * e]);
+            const float b2 = pr[32 * c + 2 * e + 1] * (__uint_as_float(u[2 * e + 1]) - sD[qc0 + 32 * c + 2 * e + 1]);
             pk[e] = pack_bf16(a, b2);
           }
-          tmem_st16(tmem + lane_base + 64 + 16 * c, pk);
-          // dS^T row t -> shared memory, 128-byte swizzle: 16-byte chunk g of box (c>>1)
+          tmem_st16(tmem + lane_base + qc0 + 32 + 16 * c, pk);
+          // dS^T row t -> box wg of shared memory, 128-byte swizzle: 16-byte chunk 4c+g
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            const int chunk = (c & 1) * 4 + g;
-            const uint32_t addr = aDSrow + (c >> 1) * L::kBox + ((chunk ^ (t & 7)) << 4);
-            st_shared_v4(addr, pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            const int chunk = 4 * c + g;
+            st_shared_v4(aDSrow + ((chunk ^ (t & 7)) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
           }
         }
         tmem_st_wait();
@@ -401,56 +417,51 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
         mbar_arrive(ds_ready);
 
         // dQ of this block (TMEM R1, lane = query row) into the fp32 accumulator: each warp
-        // stages its 32 rows in the dS^T buffer (free once the dQ product is done) as
-        // 128-byte-swizzled boxes of 32 rows x 32 floats and adds them with TMA tensor
-        // reduce-adds (one instruction per box, rows past the item clipped by the map)
+        // stages its 32 rows of its warpgroup's head-dim columns in box wg (free once the
+        // dQ product is done) as 128-byte-swizzled boxes of 32 rows x 32 floats and adds
+        // them with TMA tensor reduce-adds (rows past the item clipped by the map)
         if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
+        uint32_t uq[kHalfD / 32][32];
 #pragma unroll
-        for (int half = 0; half < D / 64; ++half) {
-          uint32_t u0[32], u1[32];
-          tmem_ld32(tmem + lane_base + 128 + 64 * half, u0);
-          tmem_ld32(tmem + lane_base + 128 + 64 * half + 32, u1);
-          tmem_ld_wait();
-          if (half == D / 64 - 1) {  // R1 fully read: the next block's dP^T may overwrite it
-            tc_fence_before();
-            mbar_arrive(dq_empty);
-          }
-          if (half > 0) {  // the previous half's boxes must have been read by the TMA
+        for (int c = 0; c < kHalfD / 32; ++c) tmem_ld32(tmem + lane_base + 128 + dc0 + 32 * c, uq[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(dq_empty);  // R1 read out: the next block's dP^T may overwrite it
+#pragma unroll
+        for (int c = 0; c < kHalfD / 32; ++c) {
+          if (c > 0) {  // the previous box of this warp must have been read by the TMA
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t off = (uint32_t)((j ^ (t & 7)) << 4);
-            st_shared_v4(aDSrow + off, u0[4 * j], u0[4 * j + 1], u0[4 * j + 2], u0[4 * j + 3]);
-            st_shared_v4(aDSrow + L::kBox + off, u1[4 * j], u1[4 * j + 1], u1[4 * j + 2], u1[4 * j + 3]);
-          }
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(aDSrow + ((j ^ (t & 7)) << 4), uq[c][4 * j], uq[c][4 * j + 1], uq[c][4 * j + 2],
+                         uq[c][4 * j + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            const int row = ib * kBlockM + (warp & 3) * 32;
-            tma_reduce_add_3d(tm_dq, sDS + (warp & 3) * 4096, 64 * half, hl, row);
-            tma_reduce_add_3d(tm_dq, sDS + L::kBox + (warp & 3) * 4096, 64 * half + 32, hl, row);
+            tma_reduce_add_3d(tm_dq, sDS + wg * L::kBox + (warp & 3) * 4096, dc0 + 32 * c, hl,
+                              ib * kBlockM + (warp & 3) * 32);
             bulk_commit();
           }
         }
         ++nblocks;
       }
       if (!ok) break;
-      // ---- dK, dV of this tile's KV rows
+      // ---- dK, dV of this tile's KV rows (this warpgroup's head-dim columns)
       if (nqb > 0) {
         if (!__all_sync(0xffffffffu, bwait(kv_done, ntiles & 1, abort_flag, p.wait_limit, p.status))) break;
         ++ntiles;
         tc_fence_after();
       }
-      const int64_t row_off = it.dkv_offset + (int64_t)kv_local * nh * D + (int64_t)hl * D;
+      const int64_t row_off = it.dkv_offset + (int64_t)kv_local * nh * D + (int64_t)hl * D + dc0;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kHalfD / 32; ++c) {
         uint32_t uv[32], uk[32];
         if (nqb > 0) {
-          tmem_ld32(tmem + lane_base + 256 + 32 * c, uv);
-          tmem_ld32(tmem + lane_base + 384 + 32 * c, uk);
+          tmem_ld32(tmem + lane_base + 256 + dc0 + 32 * c, uv);
+          tmem_ld32(tmem + lane_base + 384 + dc0 + 32 * c, uk);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -475,7 +486,7 @@ __global__ void __launch_bounds__(192, 1) zl_bwd_kernel(const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -501,9 +512,9 @@ cudaError_t launch_bwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& t
   cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
   if (head_dim == 128)
-    zl_bwd_kernel<128><<<grid, 192, smem_launch, stream>>>(tq, tk, tv, p);
+    zl_bwd_kernel<128><<<grid, 320, smem_launch, stream>>>(tq, tk, tv, p);
   else
-    zl_bwd_kernel<64><<<grid, 192, smem_launch, stream>>>(tq, tk, tv, p);
+    zl_bwd_kernel<64><<<grid, 320, smem_launch, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
