@@ -293,13 +293,15 @@ __global__ void __launch_bounds__(320, 1)
         ++sc;
         tc_fence_after();
         float s[128];
+        {
+          uint32_t u[4][32];  // all four loads in flight, one wait
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tS + 32 * c, u);
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, u[c]);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(u[e]);
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(u[c][e]);
         }
         const int valid = nkv - j * kBlockN;
         if (valid < kBlockN) {
