@@ -106,6 +106,7 @@ __device__ __forceinline__ uint32_t pcol(int kk) { return (uint32_t)((kk >> 2) *
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+
 template <int D>
 __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                         const __grid_constant__ CUtensorMap tm_k,
