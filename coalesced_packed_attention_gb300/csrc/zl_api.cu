@@ -47,20 +47,6 @@ bool make_block_map(CUtensorMap* m, const void* base, int64_t rows, int32_t H, i
   return make_qkv_map(m, base, rows, H, d);
 }
 
-// fp32 [rows, H, d] accumulator block: boxes of 32 rows x 32 floats (one 128-byte
-// swizzle span; one warp's rows), the unit of the backward's TMA reduce-adds of dQ.
-bool make_acc_map(CUtensorMap* m, const void* base, int64_t rows, int32_t H, int32_t d) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
-  cuuint32_t box[3] = {32, 1, 32};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool launchable(const zl_plan* p) { return p && !p->host_only && p->d_items; }
 
 // Spin budget of a bounded device wait: ~0.5 s at 2 GHz; short for the test hook.
@@ -121,7 +107,8 @@ extern "C" zl_status zl_bwd_preprocess(const zl_plan* p, const void* o, const vo
   float* ws_d = static_cast<float*>(workspace);
   cudaError_t e = launch_bwd_pre(p->head_dim, p->d_items, (int32_t)p->items.size(), p->total_rowheads,
                                  static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), ws_d,
-                                 ws_d + p->ws_d_floats, p->num_sms, static_cast<cudaStream_t>(stream));
+                                 ws_d + p->ws_d_floats, p->ws_dq_floats, p->num_sms,
+                                 static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
 
@@ -140,21 +127,17 @@ extern "C" zl_status zl_bwd_main(const zl_plan* p, const void* q, const void* k,
       !make_qkv_map(&tv, v, p->total_tokens, p->n_heads, p->head_dim))
     return ZL_ERR_CUDA;
   // Per item: its dO (final block in the `o` arena, [|q|, |h|, d] with row stride |h| d)
-  // and its fp32 dQ accumulator block in the workspace (same shape), for TMA loads and
-  // TMA reduce-adds.
+  // for TMA loads.
   zl_plan* mp = const_cast<zl_plan*>(p);
   float* ws_d = static_cast<float*>(workspace);
-  float* ws_dq = ws_d + p->ws_d_floats;
   for (size_t i = 0; i < p->items.size(); ++i) {
     const DevItem& it = p->items[i];
     const int64_t nq = it.q_hi - it.q_lo, nh = it.h_hi - it.h_lo;
     if (nq == 0 || nh == 0) continue;
     const void* base = static_cast<const __nv_bfloat16*>(d_o) + it.fin_out_offset;
-    if (!make_block_map(&mp->h_do_maps[2 * i], base, nq, (int32_t)nh, p->head_dim) ||
-        !make_acc_map(&mp->h_do_maps[2 * i + 1], ws_dq + it.ws_dq_offset, nq, (int32_t)nh, p->head_dim))
-      return ZL_ERR_CUDA;
+    if (!make_block_map(&mp->h_do_maps[i], base, nq, (int32_t)nh, p->head_dim)) return ZL_ERR_CUDA;
   }
-  if (cudaMemcpyAsync(p->d_do_maps, p->h_do_maps.data(), sizeof(CUtensorMap) * 2 * p->items.size(),
+  if (cudaMemcpyAsync(p->d_do_maps, p->h_do_maps.data(), sizeof(CUtensorMap) * p->items.size(),
                       cudaMemcpyHostToDevice, st) != cudaSuccess)
     return ZL_ERR_CUDA;
   BwdParams bp;

@@ -11,14 +11,31 @@
 // memory and dK_j, dV_j in TMEM while it walks the item's query blocks.  Per block:
 //   S^T  = K Q_i^T      (SMEM x SMEM -> TMEM R0)   lanes = KV rows, columns = queries
 //   dP^T = V dO_i^T     (SMEM x SMEM -> TMEM R1)
-//   softmax warpgroup (thread = KV row): P^T and dS^T in registers; bf16 copies go to
-//   TMEM R0 (P^T in columns [0,64), dS^T in [64,128)) and dS^T to shared memory
+//   softmax warpgroups (thread = KV row; each takes 64 query columns): P^T and dS^T in
+//   registers; P^T (bf16) goes to TMEM in place of S^T (R0 columns [0,32) and [64,96))
+//   and dS^T (bf16) to shared memory
 //   dV  += P^T dO_i     (TMEM x SMEM, dO read MN-major)
-//   dK  += dS^T Q_i     (TMEM x SMEM, Q read MN-major)
 //   dQ_i = dS K         (SMEM x SMEM -> TMEM R1; both operands MN-major)
-//   the same warpgroup (thread = query row) adds dQ_i to the fp32 accumulator with
-//   16-byte vector atomics; the scale is applied once when dQ is finalised.
-// TMEM (512 columns): R0 [0,128), R1 [128,256), dV [256,256+d), dK [384,384+d).
+//   dK  += dS^T Q_i     (SMEM x SMEM; dS^T read K-major, Q MN-major)
+//   the dQ warpgroup (thread = query row) reads dQ_i out of TMEM and adds it to the fp32
+//   accumulator with 16-byte vector reductions issued straight from registers; the scale
+//   is applied once when dQ is finalised.
+// The tensor pipe runs dP^T_i, dV_i, S^T_{i+1}, dQ_i, dK_i: R0 is free once dV_i has
+// read P^T and R1 once the warpgroups have read dP^T_i, so the softmax warpgroups form
+// P_{i+1} while dQ_i and dK_i run and dQ_i drains.  The drain has warps of its own
+// because an SM hands reductions to L2 at roughly 45 GB/s whichever unit issues them
+// (measured on GB300 for TMA tensor reduce-adds, bulk reduce-adds and vector `red`
+// alike): the 64 KB of one block's dQ take about as long as the block's five products,
+// so they must overlap everything else.  The drain paces its reductions over the
+// block period: issued in a burst they fill each sub-partition's memory-instruction
+// queue and hold up the TMEM loads, MMA issues and TMA issues of the warps beside them.
+// TMEM (512 columns): R0 [0,128) S^T / P^T, R1 [128,256) dP^T / dQ, dV [256,256+d),
+// dK [384,384+d).
+// Warps: 0-7 softmax (two warpgroups), 8-11 dQ drain, 12 TMA producer, 13 MMA issuer,
+// 14-15 idle.  The block is launched with 128 registers per thread (16 warps: four per
+// SM sub-partition, 16K registers each) and the warpgroups then trade registers with
+// setmaxnreg: per sub-partition 2 x 136 (softmax) + 160 (dQ) + 80 (producer / MMA) =
+// 512 = 4 x 128, exactly the launch allocation, so no increase can wait for registers.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -39,8 +56,8 @@ struct BwdLayout {
   static constexpr int kQ = kV + kTile;             // 2 stages
   static constexpr int kDO = kQ + 2 * kTile;        // 2 stages
   static constexpr int kDS = kDO + 2 * kTile;       // [128 kv][128 q] bf16, two 128-byte-swizzled boxes
-  static constexpr int kLD = kDS + 2 * kBox;        // LSE*log2(e) and D for the 128 queries of a block
-  static constexpr int kBar = kLD + 2 * 128 * 4;
+  static constexpr int kLD = kDS + 2 * kBox;        // [2 block parities] LSE*log2(e) and D of a block's 128 queries
+  static constexpr int kBar = kLD + 2 * 2 * 128 * 4;
   static constexpr int kNumBars = 21;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 64;
@@ -76,20 +93,12 @@ __device__ __forceinline__ void tensormap_acquire(const void* map) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// TMA tensor reduce-add (fp32 add into global memory) of one shared-memory box, issued
-// by one thread and tracked by its bulk-async group.
-__device__ __forceinline__ void tma_reduce_add_3d(const void* map, const void* src, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
+// Fire-and-forget fp32 add of four consecutive floats (16-byte aligned) in global memory.
+__device__ __forceinline__ void red_add_v4(float* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(__uint_as_float(a)),
+               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+               : "memory");
 }
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// The shared-memory sources of this thread's bulk groups have been read.
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// This thread's bulk groups have completed.
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Tiles of one (item, head) walk the query blocks starting at different blocks, so
 // CTAs running side by side add into different dQ rows instead of contending on one.
@@ -98,17 +107,33 @@ __device__ __forceinline__ int first_block(int step, int start, int n) {
   return b >= n ? b - n : b;
 }
 
-// TMEM column of the packed bf16 P^T for MMA K-step kk (16 queries): queries 0-63 are
-// packed by warpgroup 0 into R0 columns [0,32), queries 64-127 by warpgroup 1 into
-// [64,96); the dS^T halves sit 32 columns further on.
+// TMEM column of the packed bf16 P^T in R0 for MMA K-step kk (16 queries): queries 0-63
+// are packed by warpgroup 0 into columns [0,32), queries 64-127 by warpgroup 1 into
+// [64,96), each over S^T columns it has already read.
 __device__ __forceinline__ uint32_t pcol(int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); }
+
+// Registers per thread of a warpgroup after the split.  setmaxnreg.inc only raises and
+// setmaxnreg.dec only lowers the current count (the launch count before the first), so
+// the form is chosen from the target; the launcher checks the launch count.
+constexpr uint32_t kRegsLaunch = 128;
+constexpr uint32_t kRegsSoftmax = 136, kRegsDrain = 160, kRegsMisc = 80;
+static_assert(2 * kRegsSoftmax + kRegsDrain + kRegsMisc == 4 * kRegsLaunch,
+              "register split must equal the launch allocation");
+template <uint32_t N>
+__device__ __forceinline__ void regs_to() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg takes a multiple of 8 in [24, 256]");
+  if constexpr (N > kRegsLaunch)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+  else if constexpr (N < kRegsLaunch)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                         const __grid_constant__ CUtensorMap tm_k,
                                                         const __grid_constant__ CUtensorMap tm_v,
                                                         const BwdParams p) {
@@ -121,7 +146,7 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
   uint64_t* do_full = bar + 4;    // [2]
   uint64_t* q_empty = bar + 6;    // [2]
   uint64_t* s_full = bar + 8;     // S^T of the block in TMEM R0
-  uint64_t* ds_ready = bar + 9;   // dS^T in TMEM R0 and shared memory (128 arrivals)
+  uint64_t* ds_ready = bar + 9;   // dS^T in shared memory, dP^T read out of R1 (256 arrivals)
   uint64_t* dq_full = bar + 10;
   uint64_t* dq_empty = bar + 11;
   uint64_t* kv_done = bar + 12;
@@ -129,14 +154,13 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
   uint64_t* tile_empty = bar + 15;  // [2]
   uint64_t* drain = bar + 17;
   uint64_t* ld_full = bar + 18;   // LSE / D of a query block staged in shared memory
-  uint64_t* p_ready = bar + 19;   // P^T in TMEM R0 (128 arrivals): the dV product may start
+  uint64_t* p_ready = bar + 19;   // P^T in TMEM R0 (256 arrivals): the dV product may start
   uint64_t* dp_full = bar + 20;   // dP^T of the block in TMEM R1
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   uint32_t* tmem_slot = misc;
   volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(misc + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
-  float* sLSE = reinterpret_cast<float*>(smem + L::kLD);
-  float* sD = sLSE + 128;
+  float* sLD = reinterpret_cast<float*>(smem + L::kLD);  // block parity b: LSE at 256 b, D at 256 b + 128
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled layouts need a 1024-byte aligned base
@@ -151,26 +175,26 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
       mbar_init(do_full + i, 1);
       mbar_init(q_empty + i, 1);
       mbar_init(tile_full + i, 1);
-      mbar_init(tile_empty + i, 1 + 8);
+      mbar_init(tile_empty + i, 1 + 8 + 4);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 256);
+    mbar_init(dq_empty, 128);
     mbar_init(kv_done, 1);
     mbar_init(drain, 1);
     mbar_init(ld_full, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -184,7 +208,9 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
   uint8_t* sDO = smem + L::kDO;
   uint8_t* sDS = smem + L::kDS;
 
-  if (warp == 8) {
+  if (warp >= 12) {
+   regs_to<kRegsMisc>();
+   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t tile_it = 0, kt = 0, qit = 0;
@@ -203,7 +229,7 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
         const int nq = it.q_hi - it.q_lo;
         const int nqb = (nq + kBlockM - 1) / kBlockM;
         if (nqb == 0) continue;
-        const CUtensorMap* tm_do = p.do_maps + 2 * tl.item;
+        const CUtensorMap* tm_do = p.do_maps + tl.item;
         tensormap_acquire(tm_do);
         if (!bwait(kv_empty, (kt & 1) ^ 1, abort_flag, p.wait_limit, p.status)) break;
         ++kt;
@@ -229,7 +255,7 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
         }
       }
     }
-  } else if (warp == 9) {
+   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdSq = idesc_bf16(128, 128, false, false);
@@ -254,18 +280,22 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
         if (!bwait(kv_full, kt & 1, abort_flag, p.wait_limit, p.status)) break;
         ++kt;
         tc_fence_after();
-        for (int is = 0; is < nqb; ++is) {
-          const int ib = first_block(is, tl.block % nqb, nqb);
-          const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
-          if (!bwait(q_full + st, ph, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t aQs = aQ + st * L::kTile, aDOs = aDO + st * L::kTile;
+        // S^T = K Q^T of the query block in slot st (TMEM R0)
+        auto issue_s = [&](uint32_t st) {
+          const uint32_t aQs = aQ + st * L::kTile;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
+          for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
             mma_ss(tR0, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQs + off, 16, 1024), kIdSq, kk > 0);
           }
           mma_commit(s_full);
+        };
+        if (!bwait(q_full + (qit & 1), (qit >> 1) & 1, abort_flag, p.wait_limit, p.status)) break;
+        tc_fence_after();
+        issue_s(qit & 1);
+        for (int is = 0; is < nqb; ++is) {
+          const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
+          const uint32_t aQs = aQ + st * L::kTile, aDOs = aDO + st * L::kTile;
           if (!bwait(do_full + st, ph, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           if (nblocks > 0 && !bwait(dq_empty, (nblocks - 1) & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
@@ -282,18 +312,31 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
           for (int kk = 0; kk < 8; ++kk)  // K = 128 queries
             mma_ts(tdV, tR0 + pcol(kk), sdesc_sw128(aDOs + kk * 2048, L::kBox, 1024), kIdKV,
                    (is > 0 || kk > 0) ? 1u : 0u);
+          if (is + 1 < nqb) {
+            // S^T of the next block as soon as dV has read P^T out of R0 (one thread's
+            // products run in issue order): the softmax warpgroups start on it while
+            // this block's dK and dQ run
+            const uint32_t st2 = (qit + 1) & 1, ph2 = ((qit + 1) >> 1) & 1;
+            if (!bwait(q_full + st2, ph2, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(st2);
+          }
           if (!bwait(ds_ready, nblocks & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
+          // dQ first (R1 is free once the warpgroups have read dP^T): the drain warps start
+          // on it while dK runs
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
-            mma_ts(tdK, tR0 + 32 + pcol(kk), sdesc_sw128(aQs + kk * 2048, L::kBox, 1024), kIdKV,
-                   (is > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ = dS K   (K = 128 KV rows)
+          for (int kk = 0; kk < 8; ++kk)  // dQ = dS K   (K = 128 KV rows; both operands MN-major)
             mma_ss(tR1, sdesc_sw128(aDS + kk * 2048, L::kBox, 1024), sdesc_sw128(aK + kk * 2048, L::kBox, 1024),
                    kIdDQ, kk > 0);
-          mma_commit(q_empty + st);
           mma_commit(dq_full);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T read K-major from shared memory)
+            const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
+            mma_ss(tdK, sdesc_sw128(aDS + off, 16, 1024), sdesc_sw128(aQs + kk * 2048, L::kBox, 1024), kIdKV,
+                   (is > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(q_empty + st);
           ++qit;
           ++nblocks;
         }
@@ -304,14 +347,78 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
       mma_commit(drain);
       bwait(drain, 0, abort_flag, p.wait_limit, p.status);
     }
+   }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ drain warpgroup
+    // Thread t owns query row t of the block (TMEM lane t); for head-dim column group g
+    // (4 floats) the warp's 32 rows are 512 contiguous bytes of the tiled accumulator.
+    regs_to<kRegsDrain>();
+    constexpr int kChunks = D / 32;  // 32-column TMEM loads per row
+    constexpr int kReds = kChunks * 8;  // 16-byte reductions per row
+    // clock cycles between two reductions of a warp: the previous block period spread
+    // over slightly more than a block's reductions, within these bounds
+    constexpr long long kPaceMin = 48, kPaceMax = 160;
+    const int t = threadIdx.x & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    uint32_t tile_it = 0, nblocks = 0;
+    long long t_prev = 0;
+    for (;;) {
+      const uint32_t slot = tile_it & 1;
+      if (!__all_sync(0xffffffffu, bwait(tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.wait_limit, p.status))) break;
+      const int tid = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tile_empty + slot);
+      ++tile_it;
+      if (tid < 0) break;
+      const DevTile tl = p.tiles[tid];
+      const DevItem it = p.items[tl.item];
+      const int nq = it.q_hi - it.q_lo;
+      const int nqb = (nq + kBlockM - 1) / kBlockM;
+      float* acc = p.ws_dq + it.ws_dq_offset + (int64_t)(tl.head - it.h_lo) * nqb * (kBlockM * D) + t * 4;
+      bool ok = true;
+      for (int is = 0; is < nqb; ++is) {
+        const int ib = first_block(is, tl.block % nqb, nqb);
+        if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
+        tc_fence_after();
+        const long long t_full = clock64();
+        long long pace = t_prev > 0 ? (t_full - t_prev) / (kReds + kReds / 8) : kPaceMin;
+        pace = pace < kPaceMin ? kPaceMin : (pace > kPaceMax ? kPaceMax : pace);
+        t_prev = t_full;
+        float* dst = acc + (int64_t)ib * (kBlockM * D);
+        const bool row_ok = ib * kBlockM + t < nq;  // rows past the item hold dS = 0
+        // all of the row first: TMEM R1 is released before any reduction is issued
+        uint32_t u[kChunks][32];
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) tmem_ld32(tmem + lane_base + 128 + 32 * c, u[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(dq_empty);  // the next block's dP^T may overwrite R1
+        if (row_ok) {
+          long long t_next = clock64();
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              while (clock64() < t_next) {
+              }
+              red_add_v4(dst + (8 * c + g) * (4 * kBlockM), u[c][4 * g], u[c][4 * g + 1], u[c][4 * g + 2],
+                         u[c][4 * g + 3]);
+              t_next += pace;
+            }
+        }
+        ++nblocks;
+      }
+      if (!ok) break;
+    }
   } else {
-    // ------------------------------------------------------------ softmax / dQ warpgroups
-    // Two warpgroups share the TMEM lanes (lane = KV row for P/dS, query row for dQ) and
-    // split the columns: warpgroup wg takes queries [64wg, 64wg+64) of S^T and dP^T and
-    // head-dim columns [wg d/2, (wg+1) d/2) of dQ, dK and dV.
+    // ------------------------------------------------------------ softmax warpgroups
+    // Two warpgroups share the TMEM lanes (lane = KV row) and split the columns:
+    // warpgroup wg takes queries [64wg, 64wg+64) of S^T and dP^T and head-dim columns
+    // [wg d/2, (wg+1) d/2) of dK and dV.
+    regs_to<kRegsSoftmax>();
     constexpr int kHalfD = D / 2;
     const int wg = warp >> 2;
-    const int t = threadIdx.x & 127;  // KV row of the tile for P/dS, query row of the block for dQ
+    const int t = threadIdx.x & 127;  // KV row of the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int qc0 = 64 * wg;          // this warpgroup's query columns
     const int dc0 = kHalfD * wg;      // this warpgroup's head-dim columns
@@ -336,8 +443,6 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
       const bool kv_ok = kv_local < nkv;
       const float* lse_row = p.lse + it.fin_lse_offset + (int64_t)hl * nq;
       const float* d_row = p.ws_d + it.ws_d_offset + (int64_t)hl * nq;
-      const CUtensorMap* tm_dq = p.do_maps + 2 * tl.item + 1;  // this item's dQ accumulator
-      if (lane == 0) tensormap_acquire(tm_dq);
       bool ok = true;
       float lse_n = kInfB, d_n = 0.f;  // warpgroup 0 stages LSE / D of query t of each block
       const int ib0 = nqb > 0 ? tl.block % nqb : 0;
@@ -349,8 +454,8 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
         const int ib = first_block(is, ib0, nqb);
         // publish this block's LSE / D, prefetch the next block's
         if (wg == 0) {
-          sLSE[t] = lse_n;
-          sD[t] = d_n;
+          sLD[256 * (nblocks & 1) + t] = lse_n;
+          sLD[256 * (nblocks & 1) + 128 + t] = d_n;
         }
         mbar_arrive(ld_full);  // bounded stand-in for a barrier of both warpgroups
         if (!__all_sync(0xffffffffu, bwait(ld_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
@@ -360,6 +465,11 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
           if (is + 1 < nqb && qn < nq) { lse_n = __ldg(lse_row + qn) * kLog2eB; d_n = __ldg(d_row + qn); }
         }
 
+        // the warpgroups meet only at ld_full, so warpgroup 0 may stage the next block's
+        // LSE / D while warpgroup 1 still reads this block's: one buffer per block parity
+        // (warpgroup 0 cannot get two blocks ahead: ld_full needs both)
+        const float* sLSE = sLD + 256 * (nblocks & 1);
+        const float* sD = sLSE + 128;
         if (!__all_sync(0xffffffffu, bwait(s_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
         float pr[64];
@@ -385,11 +495,9 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
         tc_fence_before();
         mbar_arrive(p_ready);
 
+        // dP^T of this block is issued after the previous block's dQ product, which read
+        // the dS^T buffer: once dP^T is complete the buffer may be rewritten
         if (!__all_sync(0xffffffffu, bwait(dp_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
-        // this warp's rows of box wg held the previous block's dQ boxes: the TMA must
-        // have read them before they are overwritten
-        if (lane == 0) bulk_wait_read0();
-        __syncwarp();
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -403,7 +511,6 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
             const float b2 = pr[32 * c + 2 * e + 1] * (__uint_as_float(u[2 * e + 1]) - sD[qc0 + 32 * c + 2 * e + 1]);
             pk[e] = pack_bf16(a, b2);
           }
-          tmem_st16(tmem + lane_base + qc0 + 32 + 16 * c, pk);
           // dS^T row t -> box wg of shared memory, 128-byte swizzle: 16-byte chunk 4c+g
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -411,41 +518,10 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
             st_shared_v4(aDSrow + ((chunk ^ (t & 7)) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
           }
         }
-        tmem_st_wait();
         fence_proxy_async_smem();
-        tc_fence_before();
+        tc_fence_before();  // the dP^T loads are complete: dQ may overwrite R1
         mbar_arrive(ds_ready);
 
-        // dQ of this block (TMEM R1, lane = query row) into the fp32 accumulator: each warp
-        // stages its 32 rows of its warpgroup's head-dim columns in box wg (free once the
-        // dQ product is done) as 128-byte-swizzled boxes of 32 rows x 32 floats and adds
-        // them with TMA tensor reduce-adds (rows past the item clipped by the map)
-        if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
-        tc_fence_after();
-        uint32_t uq[kHalfD / 32][32];
-#pragma unroll
-        for (int c = 0; c < kHalfD / 32; ++c) tmem_ld32(tmem + lane_base + 128 + dc0 + 32 * c, uq[c]);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(dq_empty);  // R1 read out: the next block's dP^T may overwrite it
-#pragma unroll
-        for (int c = 0; c < kHalfD / 32; ++c) {
-          if (c > 0) {  // the previous box of this warp must have been read by the TMA
-            if (lane == 0) bulk_wait_read0();
-            __syncwarp();
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_v4(aDSrow + ((j ^ (t & 7)) << 4), uq[c][4 * j], uq[c][4 * j + 1], uq[c][4 * j + 2],
-                         uq[c][4 * j + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_3d(tm_dq, sDS + wg * L::kBox + (warp & 3) * 4096, dc0 + 32 * c, hl,
-                              ib * kBlockM + (warp & 3) * 32);
-            bulk_commit();
-          }
-        }
         ++nblocks;
       }
       if (!ok) break;
@@ -481,12 +557,11 @@ __global__ void __launch_bounds__(320, 1) zl_bwd_kernel(const __grid_constant__ 
       }
       tc_fence_before();
     }
-    if (lane == 0) bulk_wait0();  // every dQ reduce-add of this warp has completed
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -505,6 +580,12 @@ cudaError_t launch_bwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& t
                         ? cudaFuncSetAttribute(zl_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_launch)
                         : cudaFuncSetAttribute(zl_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_launch);
     if (e != cudaSuccess) return e;
+    // the register split adds up to exactly the launch allocation: a kernel built with
+    // another per-thread count would leave an increase waiting for registers forever
+    cudaFuncAttributes fa;
+    e = head_dim == 128 ? cudaFuncGetAttributes(&fa, zl_bwd_kernel<128>) : cudaFuncGetAttributes(&fa, zl_bwd_kernel<64>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != (int)kRegsLaunch) return cudaErrorInvalidKernelImage;
     configured[di] = true;
   }
   const int grid = p.n_tiles < num_sms ? p.n_tiles : num_sms;
@@ -512,9 +593,9 @@ cudaError_t launch_bwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& t
   cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
   if (head_dim == 128)
-    zl_bwd_kernel<128><<<grid, 320, smem_launch, stream>>>(tq, tk, tv, p);
+    zl_bwd_kernel<128><<<grid, 512, smem_launch, stream>>>(tq, tk, tv, p);
   else
-    zl_bwd_kernel<64><<<grid, 320, smem_launch, stream>>>(tq, tk, tv, p);
+    zl_bwd_kernel<64><<<grid, 512, smem_launch, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

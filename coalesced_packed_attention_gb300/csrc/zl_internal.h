@@ -1,6 +1,7 @@
 // Internal tables shared by the host planner and the kernels.
 #pragma once
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <vector>
@@ -13,6 +14,18 @@ constexpr int kBlockM = 128;   // query rows per forward tile / per backward q-s
 constexpr int kBlockN = 128;   // KV rows per forward step / per backward tile
 constexpr int kFwdBlockM = 256;  // query rows per forward tile of the two-sub-tile kernel
 
+// fp32 dQ accumulator of one item, tiled by backward query block so that one warp's
+// 16-byte vector reduction of 32 consecutive rows covers 512 contiguous bytes:
+//   acc[hl][qb][c / 4][r][c % 4]   for query q = qb * kBlockM + r, head-dim column c.
+// The last query block is padded to kBlockM rows (padding rows are never read).
+__host__ __device__ inline int64_t acc_floats(int64_t nq, int64_t nh, int64_t d) {
+  return nh * ((nq + kBlockM - 1) / kBlockM) * kBlockM * d;
+}
+__host__ __device__ inline int64_t acc_index(int64_t q, int64_t hl, int64_t c, int64_t nq, int64_t d) {
+  const int64_t nqb = (nq + kBlockM - 1) / kBlockM;
+  return ((hl * nqb + q / kBlockM) * (d / 4) + c / 4) * (4 * kBlockM) + (q % kBlockM) * 4 + (c & 3);
+}
+
 // Resolved work item as the kernels read it (device copy of the planner's table).
 struct DevItem {
   int64_t seq_offset;
@@ -24,7 +37,7 @@ struct DevItem {
   int64_t dq_offset;       // [|q|,|h|,d] block in dq
   int64_t dkv_offset;      // [|kv|,|h|,d] block in dk and dv
   int64_t ws_d_offset;     // row sums D, [|h|,|q|] floats in the workspace
-  int64_t ws_dq_offset;    // fp32 dQ accumulator, [|q|,|h|,d] floats from the accumulator base
+  int64_t ws_dq_offset;    // fp32 dQ accumulator (q-block tiled, see acc_floats) from the accumulator base
                            // (which is ws_d_floats floats into the workspace)
   int64_t rowhead_begin;   // prefix of |q|*|h| over items (row-parallel kernels)
 };
@@ -79,7 +92,7 @@ struct zl_plan {
   zl::DevGroup* d_groups = nullptr;
   zl::DevMember* d_members = nullptr;
   int32_t* d_counters = nullptr;
-  CUtensorMap* d_do_maps = nullptr;          // 2 per item (dO block, dQ accumulator block),
+  CUtensorMap* d_do_maps = nullptr;          // 1 per item (its final dO block),
                                              // rewritten by every backward call
   std::vector<CUtensorMap> h_do_maps;        // host staging of the same
 };

@@ -31,10 +31,10 @@ struct BwdParams {
   long long wait_limit;
   const float* lse;   // final LSE arena
   const float* ws_d;  // row sums D (workspace)
-  float* ws_dq;       // fp32 dQ accumulator (workspace)
+  float* ws_dq;       // fp32 dQ accumulator (workspace, tiled as acc_index)
   float* dk;
   float* dv;
-  const CUtensorMap* do_maps;  // per item: its final dO block as [|q|, |h|, d] (device memory)
+  const CUtensorMap* do_maps;  // one per item: its final dO block as [|q|, |h|, d] (device memory)
   float scale;
   float scale_log2;
 };
@@ -51,7 +51,7 @@ cudaError_t launch_merge(int head_dim, const DevGroup* groups, int32_t n_groups,
 
 cudaError_t launch_bwd_pre(int head_dim, const DevItem* items, int32_t n_items, int64_t total_rowheads,
                            const __nv_bfloat16* o, const __nv_bfloat16* d_o, float* ws_d, float* ws_dq,
-                           int num_sms, cudaStream_t stream);
+                           int64_t acc_total, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_bwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const BwdParams& p, int num_sms, cudaStream_t stream);

@@ -129,7 +129,7 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
       di.dkv_offset = dkv_next; dkv_next += align_up(nkv * nh * d, 8);
     }
     di.ws_d_offset = wsd_next; wsd_next += nq * nh;
-    di.ws_dq_offset = wsq_next; wsq_next += align_up(nq * nh * d, 8);
+    di.ws_dq_offset = wsq_next; wsq_next += acc_floats(nq, nh, d);
     di.rowhead_begin = rh; rh += nq * nh;
   }
   p->total_rowheads = rh;
@@ -224,8 +224,8 @@ zl_status upload(zl_plan* p) {
   p->d_groups = carve<DevGroup>(cur, p->groups.size());
   p->d_members = carve<DevMember>(cur, p->members.size());
   p->d_counters = carve<int32_t>(cur, kNumCounters);
-  p->d_do_maps = carve<CUtensorMap>(cur, 2 * p->items.size());
-  p->h_do_maps.resize(2 * p->items.size());
+  p->d_do_maps = carve<CUtensorMap>(cur, p->items.size());
+  p->h_do_maps.resize(p->items.size());
   auto cp = [](void* dst, const void* src, size_t n) {
     return n == 0 || cudaMemcpy(dst, src, n, cudaMemcpyHostToDevice) == cudaSuccess;
   };
@@ -352,7 +352,7 @@ extern "C" zl_status zl_plan_check_bounds(const zl_plan* p) {
       return ZL_ERR_INVALID_ARG;
     if (!in(it.dq_offset, ob, p->dq_elems) || !in(it.dkv_offset, nkv * nh * d, p->dkv_elems))
       return ZL_ERR_INVALID_ARG;
-    if (!in(it.ws_d_offset, nq * nh, p->ws_d_floats) || !in(it.ws_dq_offset, ob, p->ws_dq_floats))
+    if (!in(it.ws_d_offset, nq * nh, p->ws_d_floats) || !in(it.ws_dq_offset, acc_floats(nq, nh, d), p->ws_dq_floats))
       return ZL_ERR_INVALID_ARG;
     if (4 * (p->ws_d_floats + p->ws_dq_floats) > p->workspace_bytes) return ZL_ERR_INVALID_ARG;
   }

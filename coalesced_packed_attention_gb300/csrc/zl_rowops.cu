@@ -2,7 +2,9 @@
 // partials, the backward row sums D = rowsum(dO * O) (plus zeroing of the dQ
 // accumulator), and the dQ finalisation.  One warp per (row, head); each lane owns
 // d/32 consecutive elements, so a warp moves whole 256/512-byte rows per access and
-// consecutive warps walk consecutive rows of a [rows, heads, d] block.
+// consecutive warps walk consecutive rows of a [rows, heads, d] block.  The dQ
+// accumulator is tiled by query block (acc_index); the finalisation walks it row by
+// row within a head, so neighbouring warps read neighbouring 16-byte pieces.
 //
 // The merge is the combine that a k split of theta=(q,h,k) implies ("Zellige",
 // pith.science review, "What carries the argument"; ring attention [19] combines
@@ -129,10 +131,18 @@ template <int D>
 __global__ void __launch_bounds__(256) zl_bwd_pre_kernel(const DevItem* __restrict__ items, int32_t n_items,
                                                          int64_t total, const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ d_o,
-                                                         float* __restrict__ ws_d, float* __restrict__ ws_dq) {
+                                                         float* __restrict__ ws_d, float* __restrict__ ws_dq,
+                                                         int64_t acc_total) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  // zero the whole accumulator (a multiple of 4 floats, 16-byte aligned)
+  {
+    float4* z4 = reinterpret_cast<float4*>(ws_dq);
+    const int64_t n4 = acc_total / 4, nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += nthreads)
+      z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += nwarps) {
     const DevItem& it = items[find_segment(items, n_items, w)];
     const int nh = it.h_hi - it.h_lo, nq = it.q_hi - it.q_lo;
@@ -149,10 +159,6 @@ __global__ void __launch_bounds__(256) zl_bwd_pre_kernel(const DevItem* __restri
 #pragma unroll
     for (int k = 16; k > 0; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
     if (lane == 0) ws_d[it.ws_d_offset + (int64_t)hl * nq + row] = s;
-    Vec<D> z;
-#pragma unroll
-    for (int e = 0; e < E; ++e) z.v[e] = 0.f;
-    z.store(ws_dq + it.ws_dq_offset + vec_off);
   }
 }
 
@@ -165,13 +171,13 @@ __global__ void __launch_bounds__(256) zl_dq_finalize_kernel(const DevItem* __re
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += nwarps) {
     const DevItem& it = items[find_segment(items, n_items, w)];
-    const int nh = it.h_hi - it.h_lo;
+    const int nh = it.h_hi - it.h_lo, nq = it.q_hi - it.q_lo;
     const int64_t local = w - it.rowhead_begin;
-    const int64_t row = local / nh;
-    const int hl = (int)(local - row * nh);
+    const int hl = (int)(local / nq);
+    const int64_t row = local - (int64_t)hl * nq;
     const int64_t vec_off = (row * nh + hl) * D + lane * E;
     Vec<D> a;
-    a.load(ws_dq + it.ws_dq_offset + vec_off);
+    a.load(ws_dq + it.ws_dq_offset + acc_index(row, hl, lane * E, nq, D));
 #pragma unroll
     for (int e = 0; e < E; ++e) a.v[e] *= scale;
     a.store(dq + it.dq_offset + vec_off);
@@ -200,14 +206,14 @@ cudaError_t launch_merge(int head_dim, const DevGroup* groups, int32_t n_groups,
 }
 
 cudaError_t launch_bwd_pre(int head_dim, const DevItem* items, int32_t n_items, int64_t total,
-                           const __nv_bfloat16* o, const __nv_bfloat16* d_o, float* ws_d, float* ws_dq, int num_sms,
-                           cudaStream_t stream) {
+                           const __nv_bfloat16* o, const __nv_bfloat16* d_o, float* ws_d, float* ws_dq,
+                           int64_t acc_total, int num_sms, cudaStream_t stream) {
   if (total == 0) return cudaSuccess;
-  const int grid = row_grid(total, num_sms);
+  const int grid = row_grid(total > acc_total / 128 ? total : acc_total / 128, num_sms);
   if (head_dim == 128)
-    zl_bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(items, n_items, total, o, d_o, ws_d, ws_dq);
+    zl_bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(items, n_items, total, o, d_o, ws_d, ws_dq, acc_total);
   else
-    zl_bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(items, n_items, total, o, d_o, ws_d, ws_dq);
+    zl_bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(items, n_items, total, o, d_o, ws_d, ws_dq, acc_total);
   return cudaGetLastError();
 }
 
