@@ -220,7 +220,9 @@ def run_gpu(args):
     F_step = F_fwd + F_bwd
 
     t_plan = time.perf_counter()
-    plan = zl.zl_plan_worklist(work.items, H, d, T, zl.ZL_PLAN_FWD_ONE_SUBTILE if args.fwd_one_subtile else 0)
+    plan = zl.zl_plan_worklist(work.items, H, d, T,
+                               (zl.ZL_PLAN_FWD_ONE_SUBTILE if args.fwd_one_subtile else 0)
+                               | (zl.ZL_PLAN_FUSE_LOCAL_KMERGE if args.fuse_kmerge else 0))
     t_plan = time.perf_counter() - t_plan
 
     q, k, v, do_tok = make_inputs(T, H, d, seed=rank, with_grad_output=True, device=str(dev))
@@ -367,18 +369,19 @@ def run_gpu(args):
             "config": {"workload": work.name, "n_heads": H, "head_dim": d, "total_tokens": T,
                        "items": len(work.items), "fwd_tflop": F_fwd / 1e12, "bwd_tflop": F_bwd / 1e12,
                        "l2": "inputs larger than L2 (Q, K, V, dO 302 MB each)",
-                       "parallelism": f"replicas x{ws}"},
+                       "parallelism": f"replicas x{ws}", "fused_kmerge": bool(args.fuse_kmerge)},
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "stage_ms": {"fwd": fwd_ms, "merge": merge_ms, "bwd_preprocess": pre_ms, "bwd_main": bwd_ms,
                          "bwd_finalize": fin_ms},
-            "merge_gbs": merge_bytes / (merge_ms * 1e-3) / 1e9 if merge_ms > 0 else None,
+            "merge_gbs": merge_bytes / (merge_ms * 1e-3) / 1e9 if merge_ms > 0 and plan.n_merge_groups else None,
             "bwd_preprocess_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9 if pre_ms > 0 else None,
             "plan_ms": t_plan * 1e3,
             "roofline": {"kernel": "zl_bwd_main (tcgen05 backward)", "bound": "tensor", "achieved": bwd_tf,
                          "peak": peak, "peak_kind": f"{peak_kind} bf16 sustained", "unit": "TFLOP/s",
                          "frac": bwd_tf / peak, "traffic": traffic,
                          "fwd": {"achieved": fwd_tf, "frac": fwd_tf / peak}},
-            "gpu_launches": 5 * args.steps,
+            # forward, merge (unless every group is fused), row sums, backward, finalize
+            "gpu_launches": (4 + (1 if plan.n_merge_groups else 0)) * args.steps,
             "clocks": summarize_clocks(clock_lines, dev.index or 0),
         }
         if e2e is not None:
@@ -445,6 +448,61 @@ def run_additivity(args):
     print(json.dumps(line), flush=True)
 
 
+def run_kmerge_compare(args):
+    """Forward of the long-video list (a 147600-token video as 8 k-split chunks of
+    18450 KV tokens over all rows and heads, plus 8 whole 4096-token images), timed with
+    the chunks' fp32 partials and the merge launch, and with the group fused into the
+    forward (ZL_PLAN_FUSE_LOCAL_KMERGE: one item over the whole KV range, final O and LSE
+    written directly).  Same algorithmic FLOPs; the fused step skips writing and
+    re-reading the partials."""
+    import torch
+    from coalesced_packed_attention_gb300 import zl
+    from coalesced_packed_attention_gb300.workloads import config_long_video, make_inputs, scaled
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    work = config_long_video()
+    if args.scale > 1:
+        work = scaled(work, args.scale)
+    H, d, T, scale = work.n_heads, work.head_dim, work.total_tokens, work.scale
+    q, k, v = make_inputs(T, H, d, seed=0, device=str(dev))[:3]
+    stream = torch.cuda.current_stream(dev)
+    F = work.fwd_flops()
+    out = {"workload": work.name, "fwd_tflop": F / 1e12}
+    for name, flags in (("merged", 0), ("fused", zl.ZL_PLAN_FUSE_LOCAL_KMERGE)):
+        plan = zl.zl_plan_worklist(work.items, H, d, T, flags)
+        bufs = zl.allocate(plan, dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+        def step(record=False):
+            if record:
+                ev[0].record(stream)
+            zl.zl_coalesced_attn_fwd(plan, q, k, v, bufs["o"], bufs["o_partial"], bufs["lse"], scale, stream)
+            if record:
+                ev[1].record(stream)
+            zl.zl_merge_partials(plan, bufs["o_partial"], bufs["lse"], bufs["o"], bufs["lse"], stream)
+            if record:
+                ev[2].record(stream)
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        fwd, mrg = [], []
+        for _ in range(args.steps):
+            step(True)
+            torch.cuda.synchronize(dev)
+            fwd.append(ev[0].elapsed_time(ev[1]))
+            mrg.append(ev[1].elapsed_time(ev[2]))
+        if zl.zl_get_device_status(plan, stream) != 0:
+            raise RuntimeError("device status after the k-merge comparison")
+        ms = float(np.median(np.array(fwd) + np.array(mrg)))
+        out[name] = {"ms_per_step": ms, "fwd_ms": float(np.median(fwd)), "merge_ms": float(np.median(mrg)),
+                     "tflops": F / (ms * 1e-3) / 1e12, "o_partial_bytes": 4 * plan.o_partial_elems}
+        del bufs
+        plan.destroy()
+    out["speedup"] = out["merged"]["ms_per_step"] / out["fused"]["ms_per_step"]
+    print(json.dumps({"kmerge_compare": out}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -459,8 +517,14 @@ def main():
                     help="use the 128-row single-warpgroup forward variant")
     ap.add_argument("--additivity", action="store_true",
                     help="time every work item alone and the coalesced list (co-location check)")
+    ap.add_argument("--fuse-kmerge", action="store_true",
+                    help="plan with ZL_PLAN_FUSE_LOCAL_KMERGE (k-split groups fused into the forward)")
+    ap.add_argument("--kmerge-compare", action="store_true",
+                    help="time the long-video forward list merged and fused")
     args = ap.parse_args()
-    if args.additivity:
+    if args.kmerge_compare:
+        run_kmerge_compare(args)
+    elif args.additivity:
         run_additivity(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -58,7 +58,7 @@ extern "C" zl_status zl_coalesced_attn_fwd(const zl_plan* p, const void* q, cons
                                            float* o_partial, float* lse, float scale, void* stream) {
   if (!launchable(p) || !q || !k || !v || !lse) return ZL_ERR_INVALID_ARG;
   bool any_whole = false, any_emit = false;
-  for (const auto& it : p->items) (it.emit_lse ? any_emit : any_whole) = true;
+  for (const auto& t : p->fwd_tiles) (p->items[t.item].emit_lse ? any_emit : any_whole) = true;
   if ((any_whole && !o) || (any_emit && !o_partial)) return ZL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(o_partial) ||
       !aligned16(lse))
@@ -90,11 +90,11 @@ extern "C" zl_status zl_coalesced_attn_fwd(const zl_plan* p, const void* q, cons
 extern "C" zl_status zl_merge_partials(const zl_plan* p, const float* o_partial, const float* lse_partial, void* o,
                                        float* lse_out, void* stream) {
   if (!launchable(p)) return ZL_ERR_INVALID_ARG;
-  if (p->groups.empty()) return ZL_OK;
+  if (p->merge_groups.empty()) return ZL_OK;  // none, or all fused into the forward
   if (!o_partial || !lse_partial || !o || !lse_out) return ZL_ERR_INVALID_ARG;
   if (!aligned16(o_partial) || !aligned16(lse_partial) || !aligned16(o) || !aligned16(lse_out)) return ZL_ERR_ALIGN;
-  cudaError_t e = launch_merge(p->head_dim, p->d_groups, (int32_t)p->groups.size(), p->d_members,
-                               p->group_rowheads, o_partial, lse_partial, static_cast<__nv_bfloat16*>(o), lse_out,
+  cudaError_t e = launch_merge(p->head_dim, p->d_groups, (int32_t)p->merge_groups.size(), p->d_members,
+                               p->merge_rowheads, o_partial, lse_partial, static_cast<__nv_bfloat16*>(o), lse_out,
                                p->num_sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
@@ -105,7 +105,7 @@ extern "C" zl_status zl_bwd_preprocess(const zl_plan* p, const void* o, const vo
   if (!aligned16(o) || !aligned16(d_o) || !aligned16(workspace)) return ZL_ERR_ALIGN;
   if (p->items.empty()) return ZL_OK;
   float* ws_d = static_cast<float*>(workspace);
-  cudaError_t e = launch_bwd_pre(p->head_dim, p->d_items, (int32_t)p->items.size(), p->total_rowheads,
+  cudaError_t e = launch_bwd_pre(p->head_dim, p->d_items, p->n_user, p->total_rowheads,
                                  static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), ws_d,
                                  ws_d + p->ws_d_floats, p->ws_dq_floats, p->num_sms,
                                  static_cast<cudaStream_t>(stream));
@@ -130,14 +130,14 @@ extern "C" zl_status zl_bwd_main(const zl_plan* p, const void* q, const void* k,
   // for TMA loads.
   zl_plan* mp = const_cast<zl_plan*>(p);
   float* ws_d = static_cast<float*>(workspace);
-  for (size_t i = 0; i < p->items.size(); ++i) {
+  for (int32_t i = 0; i < p->n_user; ++i) {
     const DevItem& it = p->items[i];
     const int64_t nq = it.q_hi - it.q_lo, nh = it.h_hi - it.h_lo;
     if (nq == 0 || nh == 0) continue;
     const void* base = static_cast<const __nv_bfloat16*>(d_o) + it.fin_out_offset;
     if (!make_block_map(&mp->h_do_maps[i], base, nq, (int32_t)nh, p->head_dim)) return ZL_ERR_CUDA;
   }
-  if (cudaMemcpyAsync(p->d_do_maps, p->h_do_maps.data(), sizeof(CUtensorMap) * p->items.size(),
+  if (cudaMemcpyAsync(p->d_do_maps, p->h_do_maps.data(), sizeof(CUtensorMap) * p->n_user,
                       cudaMemcpyHostToDevice, st) != cudaSuccess)
     return ZL_ERR_CUDA;
   BwdParams bp;
@@ -164,7 +164,7 @@ extern "C" zl_status zl_bwd_finalize(const zl_plan* p, float* dq, void* workspac
   if (!aligned16(dq) || !aligned16(workspace)) return ZL_ERR_ALIGN;
   if (p->items.empty()) return ZL_OK;
   const float* ws_dq = static_cast<const float*>(workspace) + p->ws_d_floats;
-  cudaError_t e = launch_dq_finalize(p->head_dim, p->d_items, (int32_t)p->items.size(), p->total_rowheads, ws_dq,
+  cudaError_t e = launch_dq_finalize(p->head_dim, p->d_items, p->n_user, p->total_rowheads, ws_dq,
                                      dq, scale, p->num_sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }

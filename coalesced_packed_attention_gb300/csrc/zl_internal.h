@@ -76,13 +76,17 @@ struct zl_plan {
   std::vector<zl_work_item> resolved;
   std::vector<int32_t> item_group;
   std::vector<zl::DevTile> fwd_tiles, bwd_tiles;
-  std::vector<zl::DevGroup> groups;
+  std::vector<zl::DevGroup> groups;        // every merge group (queries)
+  std::vector<zl::DevGroup> merge_groups;  // the groups the merge launch combines (unfused)
+  std::vector<uint8_t> group_fused;        // per group: computed as one forward item
   std::vector<zl::DevMember> members;
   std::vector<int32_t> member_items;
 
   int64_t o_elems = 0, o_partial_elems = 0, lse_elems = 0, dq_elems = 0, dkv_elems = 0;
   int64_t ws_d_floats = 0, ws_dq_floats = 0, workspace_bytes = 0;
-  int64_t total_rowheads = 0, group_rowheads = 0;
+  int64_t total_rowheads = 0, group_rowheads = 0, merge_rowheads = 0;
+  int32_t n_user = 0;        // work-list items; items[n_user..] are fused forward items
+  bool fuse_kmerge = false;  // ZL_PLAN_FUSE_LOCAL_KMERGE
 
   // device copies (one allocation, carved)
   void* dev_blob = nullptr;

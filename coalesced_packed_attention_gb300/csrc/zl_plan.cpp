@@ -66,13 +66,23 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
     gmembers[g].push_back(i);
     p->item_group[i] = g;
   }
-  for (auto& m : gmembers) {  // KV chunks of one group must be disjoint
+  // KV chunks of one group must be disjoint; with ZL_PLAN_FUSE_LOCAL_KMERGE a group
+  // whose chunks tile one contiguous range [kv_lo, kv_hi) is computed as one item
+  std::vector<std::pair<int32_t, int32_t>> gspan(gmembers.size(), {0, 0});
+  p->group_fused.assign(gmembers.size(), 0);
+  for (size_t g = 0; g < gmembers.size(); ++g) {
     std::vector<std::pair<int32_t, int32_t>> r;
-    for (int32_t i : m) r.push_back({items[i].kv_lo, items[i].kv_hi});
+    for (int32_t i : gmembers[g]) r.push_back({items[i].kv_lo, items[i].kv_hi});
     std::sort(r.begin(), r.end());
-    for (size_t j = 1; j < r.size(); ++j)
+    bool contiguous = true;
+    for (size_t j = 1; j < r.size(); ++j) {
       if (r[j].first < r[j - 1].second) return ZL_ERR_INVALID_ARG;
+      if (r[j].first != r[j - 1].second) contiguous = false;
+    }
+    gspan[g] = {r.front().first, r.back().second};
+    p->group_fused[g] = p->fuse_kmerge && contiguous ? 1 : 0;
   }
+  auto fused_member = [&](int32_t i) { return p->item_group[i] >= 0 && p->group_fused[p->item_group[i]]; };
 
   // ---- arena placement
   const int64_t packed_o = T * H * (int64_t)d, packed_lse = T * H;
@@ -92,6 +102,7 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
   std::set<int64_t> packed_claim, grad_claim;
 
   p->resolved.assign(items, items + n);
+  p->n_user = n;
   p->items.resize(n);
   int64_t dq_next = packed_o, dkv_next = packed_o, wsd_next = 0, wsq_next = 0, rh = 0;
   for (int32_t i = 0; i < n; ++i) {
@@ -104,11 +115,17 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
       it.out_offset = it.seq_offset * H * d;
       it.lse_offset = it.seq_offset * H;
     }
-    if (it.out_offset < 0) {
-      if (it.emit_lse) { it.out_offset = op_next; op_next += align_up(nq * nh * d, 8); }
-      else { it.out_offset = o_next; o_next += align_up(nq * nh * d, 8); }
+    if (fused_member(i)) {
+      // computed and stored through its group's fused item: no partial O, no own LSE
+      it.out_offset = -1;
+      it.lse_offset = -1;
+    } else {
+      if (it.out_offset < 0) {
+        if (it.emit_lse) { it.out_offset = op_next; op_next += align_up(nq * nh * d, 8); }
+        else { it.out_offset = o_next; o_next += align_up(nq * nh * d, 8); }
+      }
+      if (it.lse_offset < 0) { it.lse_offset = lse_next; lse_next += nq * nh; }
     }
-    if (it.lse_offset < 0) { it.lse_offset = lse_next; lse_next += nq * nh; }
     di.seq_offset = it.seq_offset;
     di.seq_len = it.seq_len;
     di.q_lo = it.q_lo; di.q_hi = it.q_hi;
@@ -162,6 +179,34 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
     p->groups.push_back(G);
   }
   p->group_rowheads = grh;
+  // the merge launch covers the unfused groups only (own row-head prefix); each fused
+  // group becomes one forward item after the work list's items, whose O (bf16) and
+  // LSE land straight in the group's final blocks
+  p->merge_groups.clear();
+  int64_t mrh = 0;
+  for (size_t g = 0; g < p->groups.size(); ++g) {
+    DevGroup G = p->groups[g];
+    if (p->group_fused[g]) {
+      const zl_work_item& f = p->resolved[gmembers[g][0]];
+      DevItem fi{};
+      fi.seq_offset = f.seq_offset;
+      fi.seq_len = f.seq_len;
+      fi.q_lo = f.q_lo; fi.q_hi = f.q_hi;
+      fi.h_lo = f.h_lo; fi.h_hi = f.h_hi;
+      fi.kv_lo = gspan[g].first; fi.kv_hi = gspan[g].second;
+      fi.emit_lse = 0;
+      fi.out_offset = fi.fin_out_offset = G.out_offset;
+      fi.lse_offset = fi.fin_lse_offset = G.lse_offset;
+      fi.dq_offset = fi.dkv_offset = -1;  // forward only
+      fi.rowhead_begin = rh;              // past every work-list row-head
+      p->items.push_back(fi);
+      continue;
+    }
+    G.rowhead_begin = mrh;
+    mrh += (int64_t)G.nq * G.nh;
+    p->merge_groups.push_back(G);
+  }
+  p->merge_rowheads = mrh;
 
   p->o_elems = o_next;
   p->o_partial_elems = op_next;
@@ -176,14 +221,18 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
 
   // ---- tiles, longest first (stable: ties keep work-list, head, block order)
   p->fwd_tiles.clear(); p->bwd_tiles.clear();
-  for (int32_t i = 0; i < n; ++i) {
+  for (int32_t i = 0; i < (int32_t)p->items.size(); ++i) {  // work-list items, then fused items
     const DevItem& it = p->items[i];
+    const bool user = i < n;
     const int32_t nqb = (int32_t)ceil_div(it.q_hi - it.q_lo, kBlockM);
     const int32_t nfb = (int32_t)ceil_div(it.q_hi - it.q_lo, p->fwd_block);
     const int32_t nkb = (int32_t)ceil_div(it.kv_hi - it.kv_lo, kBlockN);
+    const bool fwd = !user || !fused_member(i);
     for (int32_t h = it.h_lo; h < it.h_hi; ++h) {
-      for (int32_t b = 0; b < nfb; ++b) p->fwd_tiles.push_back({i, h, b, nkb});
-      for (int32_t b = 0; b < nkb; ++b) p->bwd_tiles.push_back({i, h, b, nqb});
+      if (fwd)
+        for (int32_t b = 0; b < nfb; ++b) p->fwd_tiles.push_back({i, h, b, nkb});
+      if (user)
+        for (int32_t b = 0; b < nkb; ++b) p->bwd_tiles.push_back({i, h, b, nqb});
     }
   }
   auto by_cost = [](const DevTile& a, const DevTile& b) { return a.cost > b.cost; };
@@ -212,16 +261,16 @@ zl_status upload(zl_plan* p) {
   const size_t bytes = align_up(sizeof(DevItem) * p->items.size(), 256) +
                        align_up(sizeof(DevTile) * p->fwd_tiles.size(), 256) +
                        align_up(sizeof(DevTile) * p->bwd_tiles.size(), 256) +
-                       align_up(sizeof(DevGroup) * p->groups.size(), 256) +
+                       align_up(sizeof(DevGroup) * p->merge_groups.size(), 256) +
                        align_up(sizeof(DevMember) * p->members.size(), 256) +
                        align_up(sizeof(int32_t) * kNumCounters, 256) +
-                       align_up(sizeof(CUtensorMap) * 2 * p->items.size(), 256);
+                       align_up(sizeof(CUtensorMap) * p->items.size(), 256);
   if (cudaMalloc(&p->dev_blob, bytes) != cudaSuccess) { p->dev_blob = nullptr; return ZL_ERR_NO_MEMORY; }
   char* cur = static_cast<char*>(p->dev_blob);
   p->d_items = carve<DevItem>(cur, p->items.size());
   p->d_fwd_tiles = carve<DevTile>(cur, p->fwd_tiles.size());
   p->d_bwd_tiles = carve<DevTile>(cur, p->bwd_tiles.size());
-  p->d_groups = carve<DevGroup>(cur, p->groups.size());
+  p->d_groups = carve<DevGroup>(cur, p->merge_groups.size());
   p->d_members = carve<DevMember>(cur, p->members.size());
   p->d_counters = carve<int32_t>(cur, kNumCounters);
   p->d_do_maps = carve<CUtensorMap>(cur, p->items.size());
@@ -232,7 +281,7 @@ zl_status upload(zl_plan* p) {
   bool ok = cp(p->d_items, p->items.data(), sizeof(DevItem) * p->items.size()) &&
             cp(p->d_fwd_tiles, p->fwd_tiles.data(), sizeof(DevTile) * p->fwd_tiles.size()) &&
             cp(p->d_bwd_tiles, p->bwd_tiles.data(), sizeof(DevTile) * p->bwd_tiles.size()) &&
-            cp(p->d_groups, p->groups.data(), sizeof(DevGroup) * p->groups.size()) &&
+            cp(p->d_groups, p->merge_groups.data(), sizeof(DevGroup) * p->merge_groups.size()) &&
             cp(p->d_members, p->members.data(), sizeof(DevMember) * p->members.size()) &&
             cudaMemset(p->d_counters, 0, sizeof(int32_t) * kNumCounters) == cudaSuccess;
   return ok ? ZL_OK : ZL_ERR_CUDA;
@@ -257,6 +306,7 @@ extern "C" zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items
   p->host_only = (flags & ZL_PLAN_HOST_ONLY) != 0;
   p->test_withhold = (flags & ZL_PLAN_TEST_WITHHOLD_LOAD) != 0;
   p->fwd_block = (flags & ZL_PLAN_FWD_ONE_SUBTILE) ? kBlockM : kFwdBlockM;
+  p->fuse_kmerge = (flags & ZL_PLAN_FUSE_LOCAL_KMERGE) != 0;
   zl_status s = build(p, items, n_items);
   if (s == ZL_OK && !p->host_only) s = upload(p);
   if (s != ZL_OK) {
@@ -289,7 +339,7 @@ extern "C" zl_status zl_plan_arena_sizes(const zl_plan* p, int64_t* o_elems, int
 extern "C" zl_status zl_plan_item(const zl_plan* p, int32_t i, zl_work_item* resolved,
                                   int64_t* fin_out_offset, int64_t* fin_lse_offset,
                                   int64_t* dq_offset, int64_t* dkv_offset, int32_t* group) {
-  if (!p || i < 0 || i >= (int32_t)p->items.size()) return ZL_ERR_INVALID_ARG;
+  if (!p || i < 0 || i >= p->n_user) return ZL_ERR_INVALID_ARG;
   if (resolved) *resolved = p->resolved[i];
   if (fin_out_offset) *fin_out_offset = p->items[i].fin_out_offset;
   if (fin_lse_offset) *fin_lse_offset = p->items[i].fin_lse_offset;
@@ -305,7 +355,8 @@ extern "C" zl_status zl_plan_count(const zl_plan* p, int32_t which, int64_t* cou
     case 0: *count = (int64_t)p->fwd_tiles.size(); return ZL_OK;
     case 1: *count = (int64_t)p->bwd_tiles.size(); return ZL_OK;
     case 2: *count = (int64_t)p->groups.size(); return ZL_OK;
-    case 3: *count = (int64_t)p->items.size(); return ZL_OK;
+    case 3: *count = (int64_t)p->n_user; return ZL_OK;
+    case 4: *count = (int64_t)p->merge_groups.size(); return ZL_OK;
     default: return ZL_ERR_INVALID_ARG;
   }
 }
@@ -346,19 +397,31 @@ extern "C" zl_status zl_plan_check_bounds(const zl_plan* p) {
     const DevItem& it = p->items[i];
     const int64_t nq = it.q_hi - it.q_lo, nh = it.h_hi - it.h_lo, nkv = it.kv_hi - it.kv_lo;
     const int64_t ob = nq * nh * d;
-    if (!in(it.out_offset, ob, it.emit_lse ? p->o_partial_elems : p->o_elems)) return ZL_ERR_INVALID_ARG;
-    if (!in(it.lse_offset, nq * nh, p->lse_elems)) return ZL_ERR_INVALID_ARG;
+    const bool user = (int32_t)i < p->n_user;
+    const bool fused_member = user && p->item_group[i] >= 0 && p->group_fused[p->item_group[i]];
+    if (fused_member) {  // no own blocks: the group's fused item writes its final ones
+      if (it.out_offset != -1 || it.lse_offset != -1) return ZL_ERR_INVALID_ARG;
+    } else {
+      if (!in(it.out_offset, ob, it.emit_lse ? p->o_partial_elems : p->o_elems)) return ZL_ERR_INVALID_ARG;
+      if (!in(it.lse_offset, nq * nh, p->lse_elems)) return ZL_ERR_INVALID_ARG;
+    }
     if (!in(it.fin_out_offset, ob, p->o_elems) || !in(it.fin_lse_offset, nq * nh, p->lse_elems))
       return ZL_ERR_INVALID_ARG;
+    if (!user) {  // a fused forward item: no gradients, no workspace
+      if (it.emit_lse) return ZL_ERR_INVALID_ARG;
+      continue;
+    }
     if (!in(it.dq_offset, ob, p->dq_elems) || !in(it.dkv_offset, nkv * nh * d, p->dkv_elems))
       return ZL_ERR_INVALID_ARG;
     if (!in(it.ws_d_offset, nq * nh, p->ws_d_floats) || !in(it.ws_dq_offset, acc_floats(nq, nh, d), p->ws_dq_floats))
       return ZL_ERR_INVALID_ARG;
     if (4 * (p->ws_d_floats + p->ws_dq_floats) > p->workspace_bytes) return ZL_ERR_INVALID_ARG;
   }
-  for (const auto& G : p->groups) {
+  for (size_t g = 0; g < p->groups.size(); ++g) {
+    const DevGroup& G = p->groups[g];
     if (!in(G.out_offset, (int64_t)G.nq * G.nh * d, p->o_elems) || !in(G.lse_offset, (int64_t)G.nq * G.nh, p->lse_elems))
       return ZL_ERR_INVALID_ARG;
+    if (p->group_fused[g]) continue;  // no partials to merge
     for (int32_t m = 0; m < G.n_members; ++m) {
       const DevMember& mb = p->members[G.member_begin + m];
       if (!in(mb.o_offset, (int64_t)G.nq * G.nh * d, p->o_partial_elems) ||
@@ -374,7 +437,7 @@ extern "C" zl_status zl_plan_check_bounds(const zl_plan* p) {
       return ZL_ERR_INVALID_ARG;
   }
   for (const auto& t : p->bwd_tiles) {
-    if (t.item < 0 || t.item >= n) return ZL_ERR_INVALID_ARG;
+    if (t.item < 0 || t.item >= p->n_user) return ZL_ERR_INVALID_ARG;
     const DevItem& it = p->items[t.item];
     if (t.head < it.h_lo || t.head >= it.h_hi || (int64_t)t.block * kBlockN >= it.kv_hi - it.kv_lo)
       return ZL_ERR_INVALID_ARG;

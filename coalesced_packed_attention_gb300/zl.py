@@ -19,6 +19,7 @@ ZL_OK, ZL_ERR_INVALID_ARG, ZL_ERR_ALIGN, ZL_ERR_CUDA, ZL_ERR_TIMEOUT, ZL_ERR_UNS
 ZL_PLAN_HOST_ONLY = 1
 ZL_PLAN_TEST_WITHHOLD_LOAD = 2
 ZL_PLAN_FWD_ONE_SUBTILE = 4
+ZL_PLAN_FUSE_LOCAL_KMERGE = 8
 
 
 class ZlError(RuntimeError):
@@ -111,6 +112,7 @@ class Plan:
         self.n_bwd_tiles = self._count(1)
         self.n_groups = self._count(2)
         self.n_items = self._count(3)
+        self.n_merge_groups = self._count(4)  # groups the merge launch combines (unfused)
 
     def _count(self, which: int) -> int:
         c = ctypes.c_int64()
@@ -290,7 +292,7 @@ def forward(plan: Plan, q, k, v, scale: float, bufs: Optional[dict] = None, stre
     """Forward of every item, then the merge of every k-split group."""
     bufs = bufs if bufs is not None else allocate(plan, q.device)
     zl_coalesced_attn_fwd(plan, q, k, v, bufs["o"], bufs["o_partial"], bufs["lse"], scale, stream)
-    if plan.n_groups:
+    if plan.n_merge_groups:
         zl_merge_partials(plan, bufs["o_partial"], bufs["lse"], bufs["o"], bufs["lse"], stream)
     return bufs
 

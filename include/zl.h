@@ -101,6 +101,18 @@ typedef struct zl_plan zl_plan;
  * of the default 256-row tiles split into two 128-row sub-tiles whose softmax
  * warpgroups alternate on the tensor core.  Both compute the same result. */
 #define ZL_PLAN_FWD_ONE_SUBTILE 4u
+/* Fused local k-merge.  A merge group (emit_lse items sharing sequence, rows and heads)
+ * whose KV chunks tile one contiguous range is computed by the forward launch as a
+ * single item over that range: its final O (bf16) and LSE go straight into the group's
+ * blocks, which is the merge's result up to rounding (softmax over the union of the
+ * chunks equals the LSE-weighted combine of the chunks; "Zellige", pith.science review,
+ * "What carries the argument", k split of theta).  The members' own partial O and LSE
+ * blocks are then neither allocated nor written (their resolved out_offset and
+ * lse_offset are -1; offsets given in the work list are ignored), and
+ * zl_merge_partials skips the group.  Groups with a gap between chunks are merged as
+ * usual.  The backward is unchanged: each member keeps its gradient ownership and reads
+ * the group's final O and LSE. */
+#define ZL_PLAN_FUSE_LOCAL_KMERGE 8u
 
 /* Validate a work list and build its tile lists (host C++), then upload them to the
  * current device.
@@ -145,7 +157,9 @@ ZL_API zl_status zl_plan_item(const zl_plan* plan, int32_t i, zl_work_item* reso
  * on host-only plans (no GPU needed). */
 ZL_API zl_status zl_plan_check_bounds(const zl_plan* plan);
 
-/* Counts: which = 0 forward tiles, 1 backward tiles, 2 merge groups, 3 items. */
+/* Counts: which = 0 forward tiles, 1 backward tiles, 2 merge groups, 3 items (of the
+ * work list), 4 merge groups that zl_merge_partials combines (2 minus those fused into
+ * the forward by ZL_PLAN_FUSE_LOCAL_KMERGE). */
 ZL_API zl_status zl_plan_count(const zl_plan* plan, int32_t which, int64_t* count);
 
 /* Copy a tile list to host memory as n x 4 int32 {item, head, block, cost}, in the

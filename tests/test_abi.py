@@ -169,7 +169,7 @@ def _all_lists():
     return lists
 
 
-@pytest.mark.parametrize("flags", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE])
+@pytest.mark.parametrize("flags", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE, zl.ZL_PLAN_FUSE_LOCAL_KMERGE])
 def test_every_plan_passes_the_bounds_dry_run(flags):
     for w in _all_lists():
         p = zl.zl_plan_worklist(w.items, w.n_heads, w.head_dim, w.total_tokens,
@@ -179,3 +179,68 @@ def test_every_plan_passes_the_bounds_dry_run(flags):
         # to whole 128-row query blocks) for every item, and nothing else
         need = sum(4 * it.nh * (it.nq + -(-it.nq // 128) * 128 * w.head_dim) for it in w.items)
         assert need <= p.workspace_bytes <= need + 16
+
+
+def _union(items):
+    return min(it.kv_lo for it in items), max(it.kv_hi for it in items)
+
+
+@pytest.mark.parametrize("make", [config_tiny, config_mixed, config_long_video])
+def test_fused_local_kmerge_plan(make):
+    # ZL_PLAN_FUSE_LOCAL_KMERGE: a merge group whose chunks tile one contiguous KV range
+    # becomes one forward item over that range; members keep only their backward role
+    w = make()
+    flags = zl.ZL_PLAN_HOST_ONLY
+    plain = zl.zl_plan_worklist(w.items, w.n_heads, w.head_dim, w.total_tokens, flags=flags)
+    fused = zl.zl_plan_worklist(w.items, w.n_heads, w.head_dim, w.total_tokens,
+                                flags=flags | zl.ZL_PLAN_FUSE_LOCAL_KMERGE)
+    fused.check_bounds()
+    groups = merge_groups(w.items)
+    assert plain.n_groups == fused.n_groups == len(groups) and plain.n_merge_groups == len(groups)
+    contiguous = []
+    for g in groups:
+        r = sorted((w.items[i].kv_lo, w.items[i].kv_hi) for i in g)
+        contiguous.append(all(a[1] == b[0] for a, b in zip(r, r[1:])))
+    assert fused.n_merge_groups == contiguous.count(False)
+    assert any(contiguous)
+    fused_members = {i for g, c in zip(groups, contiguous) if c for i in g}
+    for i in range(len(w.items)):
+        r = fused.item(i).item
+        if i in fused_members:
+            assert r.out_offset == -1 and r.lse_offset == -1
+            _, oo, lo = fused.group(fused.item(i).group)
+            assert (fused.item(i).fin_out_offset, fused.item(i).fin_lse_offset) == (oo, lo)
+        else:
+            assert r.out_offset == plain.item(i).item.out_offset
+        # the O blocks in `o` and the gradient blocks do not move (LSE blocks may: fused
+        # members reserve none of their own)
+        for f in ("fin_out_offset", "dq_offset", "dkv_offset"):
+            assert getattr(fused.item(i), f) == getattr(plain.item(i), f)
+    assert fused.lse_elems <= plain.lse_elems
+    # no partial blocks for fused members
+    need = sum(it.nq * it.nh * w.head_dim for i, it in enumerate(w.items) if it.emit_lse and i not in fused_members)
+    assert need <= fused.o_partial_elems <= need + 8 * len(w.items)
+    # forward tiles: members of fused groups have none; each fused group is one item
+    # (index >= n_items, in group order) tiled over its rows and heads with the union's cost
+    n = fused.n_items
+    tiles = fused.tiles(0)
+    assert not any(t[0] in fused_members for t in tiles)
+    fused_groups = [g for g, c in zip(groups, contiguous) if c]
+    for k, g in enumerate(fused_groups):
+        it0 = w.items[g[0]]
+        lo, hi = _union([w.items[i] for i in g])
+        mine = sorted((t[1], t[2]) for t in tiles if t[0] == n + k)
+        assert mine == sorted((h, b) for h in range(it0.h_lo, it0.h_hi) for b in range(-(-it0.nq // 256)))
+        assert {t[3] for t in tiles if t[0] == n + k} == {-(-(hi - lo) // 128)}
+    plain_tiles = [t for t in plain.tiles(0) if t[0] not in fused_members]
+    assert sorted(t for t in tiles if t[0] < n) == sorted(plain_tiles)
+    # backward tiles are those of the plain plan
+    assert fused.tiles(1) == plain.tiles(1)
+
+
+def test_fused_local_kmerge_leaves_gapped_groups():
+    # chunks [0,100) and [150,300) leave a gap: merged as usual
+    items = [WorkItem(0, 300, 0, 300, 0, 2, 0, 100, 1), WorkItem(0, 300, 0, 300, 0, 2, 150, 300, 1)]
+    p = zl.zl_plan_worklist(items, 2, 64, 300, flags=zl.ZL_PLAN_HOST_ONLY | zl.ZL_PLAN_FUSE_LOCAL_KMERGE)
+    assert p.n_merge_groups == 1 and all(p.item(i).item.out_offset >= 0 for i in range(2))
+    p.check_bounds()
