@@ -444,11 +444,11 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
       const float* lse_row = p.lse + it.fin_lse_offset + (int64_t)hl * nq;
       const float* d_row = p.ws_d + it.ws_d_offset + (int64_t)hl * nq;
       bool ok = true;
-      float lse_n = kInfB, d_n = 0.f;  // warpgroup 0 stages LSE / D of query t of each block
+      float lse_n = -kInfB, d_n = 0.f;  // warpgroup 0 stages -LSE*log2(e) and -D of query t of each block
       const int ib0 = nqb > 0 ? tl.block % nqb : 0;
       if (wg == 0 && nqb > 0 && ib0 * kBlockM + t < nq) {
-        lse_n = __ldg(lse_row + ib0 * kBlockM + t) * kLog2eB;
-        d_n = __ldg(d_row + ib0 * kBlockM + t);
+        lse_n = -__ldg(lse_row + ib0 * kBlockM + t) * kLog2eB;
+        d_n = -__ldg(d_row + ib0 * kBlockM + t);
       }
       for (int is = 0; is < nqb; ++is) {
         const int ib = first_block(is, ib0, nqb);
@@ -461,8 +461,8 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         if (!__all_sync(0xffffffffu, bwait(ld_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         if (wg == 0) {
           const int qn = first_block(is + 1, ib0, nqb) * kBlockM + t;
-          lse_n = kInfB; d_n = 0.f;
-          if (is + 1 < nqb && qn < nq) { lse_n = __ldg(lse_row + qn) * kLog2eB; d_n = __ldg(d_row + qn); }
+          lse_n = -kInfB; d_n = 0.f;
+          if (is + 1 < nqb && qn < nq) { lse_n = -__ldg(lse_row + qn) * kLog2eB; d_n = -__ldg(d_row + qn); }
         }
 
         // the warpgroups meet only at ld_full, so warpgroup 0 may stage the next block's
@@ -478,10 +478,18 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           tmem_ld32(tmem + lane_base + qc0, u0);
           tmem_ld32(tmem + lane_base + qc0 + 32, u1);
           tmem_ld_wait();
+          // exponent arguments two queries per instruction (the staged LSE is negated)
+          const float2 sl2v = make_float2(sl2, sl2);
+          const float2* nl2 = reinterpret_cast<const float2*>(sLSE + qc0);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            pr[e] = kv_ok ? ex2(fmaf(__uint_as_float(u0[e]), sl2, -sLSE[qc0 + e])) : 0.f;
-            pr[32 + e] = kv_ok ? ex2(fmaf(__uint_as_float(u1[e]), sl2, -sLSE[qc0 + 32 + e])) : 0.f;
+          for (int e = 0; e < 16; ++e) {
+            const float2 x0 = fma2(make_float2(__uint_as_float(u0[2 * e]), __uint_as_float(u0[2 * e + 1])), sl2v, nl2[e]);
+            const float2 x1 =
+                fma2(make_float2(__uint_as_float(u1[2 * e]), __uint_as_float(u1[2 * e + 1])), sl2v, nl2[16 + e]);
+            pr[2 * e] = kv_ok ? ex2(x0.x) : 0.f;
+            pr[2 * e + 1] = kv_ok ? ex2(x0.y) : 0.f;
+            pr[32 + 2 * e] = kv_ok ? ex2(x1.x) : 0.f;
+            pr[32 + 2 * e + 1] = kv_ok ? ex2(x1.y) : 0.f;
           }
         }
         // P^T (bf16) over this warpgroup's S^T columns, already read: dV may start now
@@ -505,11 +513,13 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           tmem_ld32(tmem + lane_base + 128 + qc0 + 32 * c, u);
           tmem_ld_wait();
           uint32_t pk[16];
+          // dS = P (dP - D), two queries per instruction (the staged D is negated)
+          const float2* nd2 = reinterpret_cast<const float2*>(sD + qc0 + 32 * c);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float a = pr[32 * c + 2 * e] * (__uint_as_float(u[2 * e]) - sD[qc0 + 32 * c + 2 * e]);
-            const float b2 = pr[32 * c + 2 * e + 1] * (__uint_as_float(u[2 * e + 1]) - sD[qc0 + 32 * c + 2 * e + 1]);
-            pk[e] = pack_bf16(a, b2);
+            const float2 ds = mul2(add2(make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1])), nd2[e]),
+                                   make_float2(pr[32 * c + 2 * e], pr[32 * c + 2 * e + 1]));
+            pk[e] = pack_bf16(ds.x, ds.y);
           }
           // dS^T row t -> box wg of shared memory, 128-byte swizzle: 16-byte chunk 4c+g
 #pragma unroll

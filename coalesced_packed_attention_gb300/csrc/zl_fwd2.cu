@@ -309,37 +309,40 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= valid) s[c] = kNegInfv;
         }
-        // row max as 8 independent chains (one warp per sub-partition per warpgroup
-        // leaves little room to hide a 128-long dependent chain)
+        // row max as 8 independent chains of three-input maxima (one warp per
+        // sub-partition per warpgroup leaves little room to hide a long dependent chain);
+        // chain e takes s[e + 8k], k = 0..15
         float mx8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(s[e], s[e + 8]);
+        for (int e = 0; e < 8; ++e) {
+          float m = max3(s[e], s[e + 8], s[e + 16]);
 #pragma unroll
-        for (int c = 16; c < 128; c += 8)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[c + e]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int k = 3; k < 15; k += 2) m = max3(m, s[e + 8 * k], s[e + 8 * k + 8]);
+          mx8[e] = fmaxf(m, s[e + 120]);
+        }
+        const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]), max3(max3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
         const float m_blk = mx * sl2;
         const bool need = m_blk > m_used + kThr;
         const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
         const float f = need ? ex2(m_used - m_blk) : 1.f;  // exp2(-inf) = 0 on the first block
         if (need) { l *= f; m_used = m_blk; }
-        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // exponent arguments and the row sum two columns per instruction; sum chain k
+        // (lane x / y) collects the columns = 2k / 2k+1 mod 8, in column order
+        float2 sum4[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        const float2 sl2v = make_float2(sl2, sl2), nm = make_float2(-m_used, -m_used);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(s[32 * c + 2 * e], sl2, -m_used));
-            const float p1 = ex2(fmaf(s[32 * c + 2 * e + 1], sl2, -m_used));
-            sum8[(2 * e) & 7] += p0;
-            sum8[(2 * e + 1) & 7] += p1;
-            pk[e] = pack_bf16(p0, p1);
+            const float2 x = fma2(make_float2(s[32 * c + 2 * e], s[32 * c + 2 * e + 1]), sl2v, nm);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            sum4[e & 3] = add2(sum4[e & 3], pp);
+            pk[e] = pack_bf16(pp.x, pp.y);
           }
           tmem_st16(tS + 16 * c, pk);
         }
-        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        l += ((sum4[0].x + sum4[0].y) + (sum4[1].x + sum4[1].y)) + ((sum4[2].x + sum4[2].y) + (sum4[3].x + sum4[3].y));
         if (rescale) {
           // S_w,j was issued after PV_w,{j-1}: its commit proves O_w stable here, and
           // PV_w,j waits for this warpgroup's P handoff below
