@@ -34,7 +34,7 @@
 // Warps: 0-7 softmax (two warpgroups), 8-11 dQ drain, 12 TMA producer, 13 MMA issuer,
 // 14-15 idle.  The block is launched with 128 registers per thread (16 warps: four per
 // SM sub-partition, 16K registers each) and the warpgroups then trade registers with
-// setmaxnreg: per sub-partition 2 x 136 (softmax) + 160 (dQ) + 80 (producer / MMA) =
+// setmaxnreg: per sub-partition 2 x 136 (softmax) + 152 (dQ) + 88 (producer / MMA) =
 // 512 = 4 x 128, exactly the launch allocation, so no increase can wait for registers.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -116,7 +116,7 @@ __device__ __forceinline__ uint32_t pcol(int kk) { return (uint32_t)((kk >> 2) *
 // setmaxnreg.dec only lowers the current count (the launch count before the first), so
 // the form is chosen from the target; the launcher checks the launch count.
 constexpr uint32_t kRegsLaunch = 128;
-constexpr uint32_t kRegsSoftmax = 136, kRegsDrain = 160, kRegsMisc = 80;
+constexpr uint32_t kRegsSoftmax = 136, kRegsDrain = 152, kRegsMisc = 88;
 static_assert(2 * kRegsSoftmax + kRegsDrain + kRegsMisc == 4 * kRegsLaunch,
               "register split must equal the launch allocation");
 template <uint32_t N>
@@ -264,6 +264,14 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
                      aDS = smem_u32(sDS);
       const uint32_t tR0 = tmem, tR1 = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      // operand descriptors built once (K-major: LBO 16 B; MN-major: LBO one 16 KB box);
+      // a K step or a ring slot only advances the start address
+      // (low words only: all share the high word, see sdesc_join)
+      const uint32_t kK = sdesc_lo(aK, 16), kV = sdesc_lo(aV, 16), kQ = sdesc_lo(aQ, 16), kDO = sdesc_lo(aDO, 16);
+      const uint32_t kDS = sdesc_lo(aDS, 16);
+      const uint32_t mK = sdesc_lo(aK, L::kBox), mQ = sdesc_lo(aQ, L::kBox), mDO = sdesc_lo(aDO, L::kBox);
+      const uint32_t mDS = sdesc_lo(aDS, L::kBox);
+      auto dsc = [](uint32_t lo, uint32_t bytes) { return sdesc_join(lo + (bytes >> 4)); };
       uint32_t tile_it = 0, kt = 0, qit = 0, nblocks = 0;
       bool ok = true;
       while (ok) {
@@ -282,11 +290,11 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         tc_fence_after();
         // S^T = K Q^T of the query block in slot st (TMEM R0)
         auto issue_s = [&](uint32_t st) {
-          const uint32_t aQs = aQ + st * L::kTile;
+          const uint32_t dq = kQ + ((st * L::kTile) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-            mma_ss(tR0, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQs + off, 16, 1024), kIdSq, kk > 0);
+            mma_ss(tR0, dsc(kK, off), dsc(dq, off), kIdSq, kk > 0);
           }
           mma_commit(s_full);
         };
@@ -295,14 +303,13 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         issue_s(qit & 1);
         for (int is = 0; is < nqb; ++is) {
           const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
-          const uint32_t aQs = aQ + st * L::kTile, aDOs = aDO + st * L::kTile;
           if (!bwait(do_full + st, ph, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           if (nblocks > 0 && !bwait(dq_empty, (nblocks - 1) & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-            mma_ss(tR1, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDOs + off, 16, 1024), kIdSq, kk > 0);
+            mma_ss(tR1, dsc(kV, off), dsc(kDO, st * L::kTile + off), kIdSq, kk > 0);
           }
           mma_commit(dp_full);
           // dV += P^T dO as soon as P^T is in TMEM (the warpgroup then forms dS^T)
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // K = 128 queries
-            mma_ts(tdV, tR0 + pcol(kk), sdesc_sw128(aDOs + kk * 2048, L::kBox, 1024), kIdKV,
+            mma_ts(tdV, tR0 + pcol(kk), dsc(mDO, st * L::kTile + kk * 2048), kIdKV,
                    (is > 0 || kk > 0) ? 1u : 0u);
           if (is + 1 < nqb) {
             // S^T of the next block as soon as dV has read P^T out of R0 (one thread's
@@ -327,13 +334,13 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           // on it while dK runs
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ = dS K   (K = 128 KV rows; both operands MN-major)
-            mma_ss(tR1, sdesc_sw128(aDS + kk * 2048, L::kBox, 1024), sdesc_sw128(aK + kk * 2048, L::kBox, 1024),
+            mma_ss(tR1, dsc(mDS, kk * 2048), dsc(mK, kk * 2048),
                    kIdDQ, kk > 0);
           mma_commit(dq_full);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T read K-major from shared memory)
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-            mma_ss(tdK, sdesc_sw128(aDS + off, 16, 1024), sdesc_sw128(aQs + kk * 2048, L::kBox, 1024), kIdKV,
+            mma_ss(tdK, dsc(kDS, off), dsc(mQ, st * L::kTile + kk * 2048), kIdKV,
                    (is > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(q_empty + st);

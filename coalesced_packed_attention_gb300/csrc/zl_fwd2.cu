@@ -190,13 +190,15 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t qcount[2] = {0, 0};  // Q sub-tile loads consumed
       uint32_t pcount[2] = {0, 0};  // P handoffs consumed per sub-tile
       bool ok = true;
+      // operand descriptors built once; a K step only advances the start address
+      const uint64_t dQ0 = sdesc_sw128(aQ, 16, 1024), dK0 = sdesc_sw128(aK, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(aV, L::kBox, 1024);
       auto issue_s = [&](int w, uint32_t stage) {
-        const uint32_t qa = aQ + w * L::kTile, ka = aK + stage * L::kTile;
+        const uint64_t dq = sdesc_add(dQ0, w * L::kTile), dk = sdesc_add(dK0, stage * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * L::kBox + (kk & 3) * 32;
-          mma_ss(tmem + 128 * w, sdesc_sw128(qa + koff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024), kIdS,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem + 128 * w, sdesc_add(dq, koff), sdesc_add(dk, koff), kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(s_full + w);
       };
@@ -204,10 +206,10 @@ __global__ void __launch_bounds__(320, 1)
         if (!wait2(p_full + w, pcount[w] & 1, abort_flag, lim, p.status)) return false;
         ++pcount[w];
         tc_fence_after();
-        const uint32_t va = aV + stage * L::kTile;
+        const uint64_t dv = sdesc_add(dV0, stage * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem + 256 + 128 * w, tmem + 128 * w + kk * 8, sdesc_sw128(va + kk * 2048, L::kBox, 1024), kIdPV,
+          mma_ts(tmem + 256 + 128 * w, tmem + 128 * w + kk * 8, sdesc_add(dv, kk * 2048), kIdPV,
                  (first && kk == 0) ? 0u : 1u);
         return true;
       };

@@ -156,6 +156,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor advanced by `bytes` (a multiple of 16): the start address is
+// the low 14-bit field and a shared-memory address stays below 256 KB, so a plain add
+// never carries into the next field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+// Low and high 32-bit words of sdesc_sw128 with SBO = 1024 B: every such descriptor
+// shares the high word, so an issuer can keep only low words (start | LBO) and join.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+constexpr uint32_t kSdescHi1024 = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo) { return ((uint64_t)kSdescHi1024 << 32) | lo; }
+
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                 // D format: f32
