@@ -503,6 +503,59 @@ def run_kmerge_compare(args):
     print(json.dumps({"kmerge_compare": out}), flush=True)
 
 
+def run_planner(args):
+    """Host placement slice (no GPU): catalog cut and filler packing of a synthetic
+    batch of 10 000 sequences (images of 256-4096 tokens, videos of 8k-147k tokens,
+    time ~ L^2, memory ~ L) over 32 ranks, the anchors q-split evenly over all ranks;
+    the library against the Python oracle on the same input."""
+    import random
+    import oracle.placement as OP
+    from coalesced_packed_attention_gb300 import zl
+
+    rng = random.Random(0)
+    img = [256, 512, 1024, 2048, 4096]
+    vid = [8190, 16380, 32760, 65520, 147600]
+    lengths = [rng.choice(img) for _ in range(9600)] + [rng.choice(vid) for _ in range(400)]
+    N, H, d = 32, 24, 128
+    t_of = lambda L: 3.5 * 4.0 * L * L * d * H / 1.3e15   # noqa: E731  seconds at ~1.3 PFLOP/s
+    m_of = lambda L: 10.0 * L * H * d * 2 / 1e9          # noqa: E731  GB, ten [L, H, d] bf16 tensors
+    counts = {}
+    for L in lengths:
+        counts[L] = counts.get(L, 0) + 1
+    cat = sorted(((L, n, t_of(L), m_of(L)) for L, n in counts.items()), key=lambda b: (b[2], b[0]))
+
+    # inputs of the packing: the anchors' per-rank load (q-split evenly) and the fillers
+    k, _ = zl.catalog_cut(cat)
+    fl = {b[0] for b in cat[:k]}
+    anchor_t = sum(t_of(L) for L in lengths if L not in fl) / N
+    anchor_m = sum(m_of(L) for L in lengths if L not in fl) / N
+    rt, rm = [anchor_t] * N, [anchor_m] * N
+    ft = [t_of(L) for L in lengths if L in fl]
+    fm = [m_of(L) for L in lengths if L in fl]
+
+    def lib_run():  # the two library calls, argument marshalling included
+        kk, _ = zl.catalog_cut(cat)
+        return kk, zl.pack_fillers(ft, fm, N, rt, rm, 0.0, 180.0)
+
+    for _ in range(3):
+        lib_run()
+    reps = 50
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        k, res = lib_run()
+    lib_ms = (time.perf_counter() - t0) * 1e3 / reps
+    t0 = time.perf_counter()
+    k_ref, _ = OP.catalog_cut([b[2] for b in cat], [b[1] for b in cat])
+    ref = OP.pack_fillers(ft, fm, N, rt, rm, 0.0, 180.0)
+    oracle_ms = (time.perf_counter() - t0) * 1e3
+    lb = max(max(rt), (sum(rt) + sum(ft)) / N)
+    print(json.dumps({"planner": {
+        "sequences": len(lengths), "ranks": N, "buckets": len(cat), "k_star": k, "fillers": len(ft),
+        "library_ms": lib_ms, "oracle_ms": oracle_ms, "same_result": bool(k == k_ref and res[0] == ref[0]),
+        "makespan_s": res[4], "lower_bound_s": lb, "makespan_over_lower_bound": res[4] / lb,
+        "overflow": res[3]}}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -521,8 +574,12 @@ def main():
                     help="plan with ZL_PLAN_FUSE_LOCAL_KMERGE (k-split groups fused into the forward)")
     ap.add_argument("--kmerge-compare", action="store_true",
                     help="time the long-video forward list merged and fused")
+    ap.add_argument("--planner", action="store_true",
+                    help="time the host placement slice (catalog cut, filler packing) on a synthetic batch")
     args = ap.parse_args()
-    if args.kmerge_compare:
+    if args.planner:
+        run_planner(args)
+    elif args.kmerge_compare:
         run_kmerge_compare(args)
     elif args.additivity:
         run_additivity(args)

@@ -37,6 +37,11 @@ class zl_work_item(ctypes.Structure):
                 ("out_offset", ctypes.c_int64), ("lse_offset", ctypes.c_int64)]
 
 
+class zl_bucket(ctypes.Structure):
+    _fields_ = [("seq_len", ctypes.c_int64), ("count", ctypes.c_int32), ("time", ctypes.c_double),
+                ("mem", ctypes.c_double)]
+
+
 _lib = None
 
 
@@ -51,6 +56,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L = ctypes.CDLL(path)
     P, I32, I64, U32, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_float
     pI64, pI32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+    pD = ctypes.POINTER(ctypes.c_double)
     sig = {
         "zl_plan_worklist": (I32, [ctypes.POINTER(zl_work_item), I32, I32, I32, I64, U32, ctypes.POINTER(P)]),
         "zl_plan_destroy": (None, [P]),
@@ -69,6 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "zl_get_device_status": (I32, [P, P, pI32]),
         "zl_status_string": (ctypes.c_char_p, [I32]),
         "zl_version": (I32, []),
+        "zl_catalog_cut": (I32, [ctypes.POINTER(zl_bucket), I32, pI32, ctypes.POINTER(ctypes.c_double)]),
+        "zl_pack_fillers": (I32, [pD, pD, I32, I32, pD, pD, ctypes.c_double, ctypes.c_double, pI32, pD, pD, pI32, pD]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -309,4 +317,32 @@ def exported_symbols() -> List[str]:
             "zl_plan_count",
             "zl_plan_tiles", "zl_plan_group", "zl_coalesced_attn_fwd", "zl_merge_partials",
             "zl_coalesced_attn_bwd", "zl_bwd_preprocess", "zl_bwd_main", "zl_bwd_finalize",
-            "zl_get_device_status", "zl_status_string", "zl_version"]
+            "zl_get_device_status", "zl_status_string", "zl_version", "zl_catalog_cut", "zl_pack_fillers"]
+
+
+# ---------------------------------------------------------------- host placement slice
+def catalog_cut(buckets):
+    """zl_catalog_cut over [(seq_len, count, time, mem), ...] sorted by time: returns
+    (k_star, dispersion); buckets[:k_star] are fillers, the rest anchors."""
+    arr = (zl_bucket * len(buckets))(*[zl_bucket(int(L), int(n), float(t), float(m)) for (L, n, t, m) in buckets])
+    k = ctypes.c_int32()
+    disp = ctypes.c_double()
+    _check(load_library().zl_catalog_cut(arr, len(buckets), ctypes.byref(k), ctypes.byref(disp)), "zl_catalog_cut")
+    return k.value, disp.value
+
+
+def pack_fillers(filler_time, filler_mem, n_ranks, rank_time=None, rank_mem=None, F=0.0, M_cap=1.0):
+    """zl_pack_fillers: returns (assign, final_time, final_mem, n_overflow, makespan)."""
+    D = ctypes.c_double
+    n = len(filler_time)
+    ft = (D * max(n, 1))(*map(float, filler_time))
+    fm = (D * max(n, 1))(*map(float, filler_mem))
+    rt = (D * n_ranks)(*map(float, rank_time)) if rank_time is not None else None
+    rm = (D * n_ranks)(*map(float, rank_mem)) if rank_mem is not None else None
+    assign = (ctypes.c_int32 * max(n, 1))()
+    out_t, out_m = (D * n_ranks)(), (D * n_ranks)()
+    over, mk = ctypes.c_int32(), D()
+    _check(load_library().zl_pack_fillers(ft, fm, n, n_ranks, rt, rm, float(F), float(M_cap), assign, out_t, out_m,
+                                          ctypes.byref(over), ctypes.byref(mk)), "zl_pack_fillers")
+    return list(assign[:n]), list(out_t), list(out_m), over.value, mk.value
+

@@ -261,6 +261,53 @@ ZL_API const char* zl_status_string(zl_status status);
 /* Library version, e.g. 100 for 0.1.0. */
 ZL_API int32_t zl_version(void);
 
+/* ------------------------------------------------------------------------------------
+ * Host placement slice (no GPU): the catalog cut and the filler packing of the
+ * two-stage planner ("Zellige", pith.science review: the catalog cut minimises the
+ * within-set dispersion of log whole-sequence times, a Fisher grouping; Filler Packing
+ * places whole sequences greedily by a bottleneck score that divides compute slack by
+ * F and memory slack by M_cap).  The anchors' own placement (an exact CP-SAT model in
+ * the pages) is not part of this library: the packing takes the anchors' per-rank time
+ * and memory as given.
+ * ---------------------------------------------------------------------------------- */
+
+/* One bucket of a sequence catalog: sequences of one length, how many there are in the
+ * batch, and the time and memory of one such sequence run whole on one rank. */
+typedef struct {
+  int64_t seq_len;
+  int32_t count;  /* >= 1 */
+  double time;    /* > 0, finite */
+  double mem;     /* >= 0 */
+} zl_bucket;
+
+/* Catalog cut.  buckets[n_buckets] sorted by time ascending (host memory, read only).
+ * With x_b = ln time_b and the count-weighted means mu_F, mu_A of x over buckets
+ * [0, k) and [k, n), the cut k in 1..n-1 minimises
+ *   D(k) = sum_{b<k} count_b (x_b - mu_F)^2 + sum_{b>=k} count_b (x_b - mu_A)^2;
+ * *k_star = that k (smallest on ties): buckets [0, k*) are fillers, [k*, n) anchors.
+ * A single bucket gives k* = 1 (all fillers), D = 0.  *dispersion (may be NULL)
+ * receives D(k*).  ZL_ERR_INVALID_ARG for n < 1, a count < 1, a time not positive and
+ * finite, or buckets out of order. */
+ZL_API zl_status zl_catalog_cut(const zl_bucket* buckets, int32_t n_buckets, int32_t* k_star, double* dispersion);
+
+/* Filler packing.  Places fillers s = 0..n_fillers-1 (time filler_time[s], memory
+ * filler_mem[s]; host arrays) whole on n_ranks ranks that already carry rank_time[r],
+ * rank_mem[r] (the anchors' load; NULL = zeros).  Fillers go in decreasing time (ties:
+ * lower index first), each to the rank with the largest bottleneck score
+ *   min((F - L_r - t) / F, (M_cap - M_r - m) / M_cap)     (ties: lowest rank)
+ * with L_r, M_r the rank's time and memory so far.  A filler whose best score is below
+ * -1e-9 (negative beyond the rounding of an exact fit) is placed all the same and
+ * counted in *n_overflow.  F <= 0 selects
+ * max(max_r rank_time[r], (sum_r rank_time[r] + sum_s filler_time[s]) / n_ranks).
+ * Outputs (host): assign[n_fillers] the rank of each filler; final_time[n_ranks] and
+ * final_mem[n_ranks] (may be NULL); *n_overflow, *makespan = max_r final time (may be
+ * NULL).  ZL_ERR_INVALID_ARG for n_ranks < 1, M_cap not positive and finite, F not
+ * finite, or a negative or non-finite time or memory. */
+ZL_API zl_status zl_pack_fillers(const double* filler_time, const double* filler_mem, int32_t n_fillers,
+                                 int32_t n_ranks, const double* rank_time, const double* rank_mem, double F,
+                                 double M_cap, int32_t* assign, double* final_time, double* final_mem,
+                                 int32_t* n_overflow, double* makespan);
+
 #ifdef __cplusplus
 }
 #endif
