@@ -458,7 +458,6 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         d_n = -__ldg(d_row + ib0 * kBlockM + t);
       }
       for (int is = 0; is < nqb; ++is) {
-        const int ib = first_block(is, ib0, nqb);
         // publish this block's LSE / D, prefetch the next block's
         if (wg == 0) {
           sLD[256 * (nblocks & 1) + t] = lse_n;
