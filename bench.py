@@ -455,6 +455,49 @@ def run_additivity(args):
     print(json.dumps(line), flush=True)
 
 
+def run_forward_configs(args):
+    """Forward (+ merge) TFLOP/s of the forward-only work lists: 64 whole images
+    (48 x 256, 12 x 1024, 4 x 4096 tokens), the mixed list (16 x 1024-token images with
+    q/h/k shards of a 32760-token video and the complementary k chunk), and the
+    147600-token video as 8 k chunks beside 8 x 4096-token images.  Median of the steps;
+    one JSON line per list."""
+    import torch
+    from coalesced_packed_attention_gb300 import zl
+    from coalesced_packed_attention_gb300.workloads import (config_images, config_long_video, config_mixed,
+                                                            make_inputs)
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    for work in (config_images(), config_mixed(), config_long_video()):
+        H, d, T, scale = work.n_heads, work.head_dim, work.total_tokens, work.scale
+        q, k, v = make_inputs(T, H, d, seed=0, device=str(dev))[:3]
+        plan = zl.zl_plan_worklist(work.items, H, d, T)
+        bufs = zl.allocate(plan, dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        times = []
+        for s in range(args.warmup + args.steps):
+            ev[0].record(stream)
+            zl.zl_coalesced_attn_fwd(plan, q, k, v, bufs["o"], bufs["o_partial"], bufs["lse"], scale, stream)
+            ev[1].record(stream)
+            zl.zl_merge_partials(plan, bufs["o_partial"], bufs["lse"], bufs["o"], bufs["lse"], stream)
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            if s >= args.warmup:
+                times.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
+        if zl.zl_get_device_status(plan, stream) != 0:
+            raise RuntimeError(f"device status after {work.name}")
+        f_ms = float(np.median([a for a, _ in times]))
+        m_ms = float(np.median([b for _, b in times]))
+        F = work.fwd_flops()
+        print(json.dumps({"forward_config": {
+            "workload": work.name, "fwd_tflop": F / 1e12, "fwd_ms": f_ms, "merge_ms": m_ms,
+            "tflops_fwd_plus_merge": F / ((f_ms + m_ms) * 1e-3) / 1e12, "tflops_fwd": F / (f_ms * 1e-3) / 1e12,
+            "fwd_tiles": plan.n_fwd_tiles}}), flush=True)
+        del bufs, q, k, v
+        plan.destroy()
+
+
 def run_kmerge_compare(args):
     """Forward of the long-video list (a 147600-token video as 8 k-split chunks of
     18450 KV tokens over all rows and heads, plus 8 whole 4096-token images), timed with
@@ -581,11 +624,15 @@ def main():
                     help="plan with ZL_PLAN_FUSE_LOCAL_KMERGE (k-split groups fused into the forward)")
     ap.add_argument("--kmerge-compare", action="store_true",
                     help="time the long-video forward list merged and fused")
+    ap.add_argument("--forward-configs", action="store_true",
+                    help="forward (+ merge) TFLOP/s of the images, mixed and long-video lists")
     ap.add_argument("--planner", action="store_true",
                     help="time the host placement slice (catalog cut, filler packing) on a synthetic batch")
     args = ap.parse_args()
     if args.planner:
         run_planner(args)
+    elif args.forward_configs:
+        run_forward_configs(args)
     elif args.kmerge_compare:
         run_kmerge_compare(args)
     elif args.additivity:
