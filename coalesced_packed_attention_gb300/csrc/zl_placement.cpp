@@ -1,9 +1,10 @@
 // Host placement slice of the two-stage planner (no GPU): the catalog cut that
 // separates anchor buckets from filler buckets, and the greedy packing of whole filler
 // sequences into the per-rank headroom left by the anchors ("Zellige", pith.science
-// review: the catalog cut minimises the within-set dispersion of log whole-sequence
-// times, a Fisher grouping; Filler Packing places whole sequences greedily by a
-// bottleneck score that divides compute slack by F and memory slack by M_cap).
+// review, "Free parameters" and the referee report on Eq. (8): the cut is the Fisher
+// grouping under which the log run times of whole sequences vary least inside each
+// set; a filler goes to the rank whose tighter resource, compute headroom against F or
+// memory headroom against M_cap, stays the most open).
 //
 // Catalog cut.  Buckets sorted by whole-sequence time T_1 <= ... <= T_B, bucket b
 // holding n_b sequences.  For a cut k in 1..B-1 the fillers are buckets 1..k and the

@@ -3,9 +3,9 @@
 //
 // The work list mixes whole sequences with theta=(q,h,k) shards co-located on one
 // rank ("Zellige", pith.science review, "What carries the argument"); the planner is
-// what lets one launch "stably schedule and fuse" them: tiles from every item share a
-// single list, ordered by cost with work-list order breaking ties, so the schedule is
-// deterministic for a given list.
+// what lets one launch run them together in a reproducible order: tiles from every item
+// share a single list, ordered by cost with work-list order breaking ties, so the
+// schedule is deterministic for a given list.
 #include <cuda_runtime.h>
 
 #include <algorithm>

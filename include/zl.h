@@ -263,10 +263,11 @@ ZL_API int32_t zl_version(void);
 
 /* ------------------------------------------------------------------------------------
  * Host placement slice (no GPU): the catalog cut and the filler packing of the
- * two-stage planner ("Zellige", pith.science review: the catalog cut minimises the
- * within-set dispersion of log whole-sequence times, a Fisher grouping; Filler Packing
- * places whole sequences greedily by a bottleneck score that divides compute slack by
- * F and memory slack by M_cap).  The anchors' own placement (an exact CP-SAT model in
+ * two-stage planner ("Zellige", pith.science review, "Free parameters" and the referee
+ * report on Eq. (8): the cut is the Fisher grouping under which the log run times of
+ * whole sequences vary least inside each set; a filler goes to the rank whose tighter
+ * resource, compute headroom against F or memory headroom against M_cap, stays the
+ * most open).  The anchors' own placement (an exact CP-SAT model in
  * the pages) is not part of this library: the packing takes the anchors' per-rank time
  * and memory as given.
  * ---------------------------------------------------------------------------------- */

@@ -5,14 +5,14 @@ module.  It shares no code with the C++ slice and imports nothing from the packa
 
 What it computes (method: "Zellige: Moldable Sequence Placement for Mixed Image-Video
 DiT Training"; the pages name both rules without printing them):
-  * Catalog cut (pith.science review, "Free parameters": the cut k* is chosen by
-    minimising the within-set dispersion of log whole-sequence times, a Fisher grouping,
-    ref. [28]).  Reading: buckets sorted by whole-sequence time T; every sequence is one
+  * Catalog cut (pith.science review, "Free parameters", and its ref. [28], Fisher's
+    grouping: the cut is the split under which the log run times of whole sequences
+    vary least inside each set).  Reading: buckets sorted by whole-sequence time T; every sequence is one
     observation x = ln T; the dispersion of a cut is the sum over the two sets of the
     squared deviations from each set's mean; the set below the cut holds the fillers.
-  * Filler Packing (pith.science review, "Major comments" on Eq. (8): the score divides
-    compute slack by F and memory slack by M_cap; "What carries the argument": whole
-    filler sequences are packed greedily by a bottleneck score).  Reading: fillers in
+  * Filler Packing (pith.science review, referee report on Eq. (8), and "What carries
+    the argument": whole fillers are placed one by one, scored by their tighter
+    resource, compute headroom normalised by F or memory headroom by M_cap).  Reading: fillers in
     decreasing time, each to the rank whose smaller normalised slack after taking it is
     largest; F defaults to the makespan lower bound.
 Ties: smallest cut; earlier filler first; lowest rank.
