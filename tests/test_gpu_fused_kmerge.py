@@ -17,19 +17,21 @@ FUSE = zl.ZL_PLAN_FUSE_LOCAL_KMERGE
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_fused_edges_all_rows(d):
+@pytest.mark.parametrize("variant", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE])
+def test_fused_edges_all_rows(d, variant):
     # a 3-way k split with an empty, unaligned middle chunk, beside whole and
-    # degenerate items
+    # degenerate items; both forward kernels
     H = 3
     w = Workload(f"edges_d{d}", H, d, 300, tiny_edge_items(H), d ** -0.5)
-    r = Run(w, seed=5, flags=FUSE)
+    r = Run(w, seed=5, flags=FUSE | variant)
     assert r.plan.n_merge_groups == 0 and r.plan.n_groups == 1
     r.check_forward()
 
 
-def test_fused_long_video_sampled_rows():
+@pytest.mark.parametrize("variant", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE])
+def test_fused_long_video_sampled_rows(variant):
     # 8 chunks of a video (lengths / 8) fused into one item of the whole KV range
-    r = Run(scaled(config_long_video(), 8), seed=6, flags=FUSE)
+    r = Run(scaled(config_long_video(), 8), seed=6, flags=FUSE | variant)
     assert r.plan.n_merge_groups == 0
     r.check_forward(sample=1024)
 
