@@ -196,16 +196,17 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t tile_it = 0, kv_it = 0, q_it = 0, sc = 0;
       bool ok = true;
       // O += P_jj V_jj, P read from the S buffer the softmax overwrote with bf16.
+      // operand descriptors built once; a K step or a ring slot only advances the start
+      const uint64_t dQ = sdesc_sw128(aQ, 16, 1024), dK0 = sdesc_sw128(aK, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(aV, L::kBox, 1024);
       auto issue_pv = [&](uint32_t stage, uint32_t kvph, uint32_t scc, bool first) -> bool {
         if (!wait_or_abort(b.p_full + (scc & 1), (scc >> 1) & 1, abort_flag, p.wait_limit, p.status)) return false;
         if (!wait_or_abort(b.v_full + stage, kvph, abort_flag, p.wait_limit, p.status)) return false;
         tc_fence_after();
         const uint32_t tP = tmem + (scc & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(aV + stage * L::kTile + kk * 2048, L::kBox, 1024);
-          mma_ts(tO, tP + kk * 8, bd, kIdescPV, (first && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ts(tO, tP + kk * 8, sdesc_add(dV0, stage * L::kTile + kk * 2048), kIdescPV, (first && kk == 0) ? 0u : 1u);
         mma_commit(b.v_empty + stage);
         mma_commit(b.o_bar);
         return true;
@@ -233,9 +234,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * L::kBox + (kk & 3) * 32;
-            const uint64_t ad = sdesc_sw128(aQ + koff, 16, 1024);
-            const uint64_t bd = sdesc_sw128(aK + s * L::kTile + koff, 16, 1024);
-            mma_ss(tS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss(tS, sdesc_add(dQ, koff), sdesc_add(dK0, s * L::kTile + koff), kIdescS, kk > 0 ? 1u : 0u);
           }
           mma_commit(b.k_empty + s);
           mma_commit(b.s_full + (sc & 1));
@@ -283,26 +282,32 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const uint32_t tS = tmem + lane_base + buf * 128;
         float s[128];
+        {
+          uint32_t u[4][32];  // all four loads in flight, one wait
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tS + 32 * c, u);
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, u[c]);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(u[e]);
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(u[c][e]);
         }
         const int valid = nkv - j * kBlockN;  // columns >= valid are past the chunk
-        float mx = kNegInf;
-        if (valid >= kBlockN) {
+        if (valid < kBlockN) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) {
+          for (int c = 0; c < 128; ++c)
             if (c >= valid) s[c] = kNegInf;
-            mx = fmaxf(mx, s[c]);
-          }
         }
+        // row max as 8 chains of three-input maxima; chain e takes s[e + 8k], k = 0..15
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float m = max3(s[e], s[e + 8], s[e + 16]);
+#pragma unroll
+          for (int k = 3; k < 15; k += 2) m = max3(m, s[e + 8 * k], s[e + 8 * k + 8]);
+          mx8[e] = fmaxf(m, s[e + 120]);
+        }
+        const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]), max3(max3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
         const float m_blk = mx * sl2;
         const bool need = m_blk > m_used + kRescaleThreshold;
         bool waited = false;
@@ -326,20 +331,22 @@ __global__ void __launch_bounds__(192, 1)
         } else if (need) {
           m_used = m_blk;  // first block: O is overwritten by the first PV product
         }
-        float sum = 0.f;
+        // exponent arguments and the row sum two columns per instruction (four chains)
+        float2 sum4[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        const float2 sl2v = make_float2(sl2, sl2), nm = make_float2(-m_used, -m_used);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t pk[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2(fmaf(s[64 * c + 2 * e], sl2, -m_used));
-            const float p1 = ex2(fmaf(s[64 * c + 2 * e + 1], sl2, -m_used));
-            sum += p0 + p1;
-            pk[e] = pack_bf16(p0, p1);
+            const float2 x = fma2(make_float2(s[64 * c + 2 * e], s[64 * c + 2 * e + 1]), sl2v, nm);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            sum4[e & 3] = add2(sum4[e & 3], pp);
+            pk[e] = pack_bf16(pp.x, pp.y);
           }
           tmem_st32(tS + 32 * c, pk);
         }
-        l += sum;
+        l += ((sum4[0].x + sum4[0].y) + (sum4[1].x + sum4[1].y)) + ((sum4[2].x + sum4[2].y) + (sum4[3].x + sum4[3].y));
         tmem_st_wait();
         if (j > 0 && !waited) {
           if (!__all_sync(0xffffffffu, wait_or_abort(b.o_bar, pv_seen & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
