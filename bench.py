@@ -556,10 +556,9 @@ def run_kmerge_compare(args):
 def run_planner(args):
     """Host placement slice (no GPU): catalog cut and filler packing of a synthetic
     batch of 10 000 sequences (images of 256-4096 tokens, videos of 8k-147k tokens,
-    time ~ L^2, memory ~ L) over 32 ranks, the anchors q-split evenly over all ranks;
-    the library against the Python oracle on the same input."""
+    time ~ L^2, memory ~ L) over 32 ranks, the anchors q-split evenly over all ranks
+    (parity with the oracle is checked by the tests, not here)."""
     import random
-    import oracle.placement as OP
     from coalesced_packed_attention_gb300 import zl
 
     rng = random.Random(0)
@@ -594,16 +593,11 @@ def run_planner(args):
     for _ in range(reps):
         k, res = lib_run()
     lib_ms = (time.perf_counter() - t0) * 1e3 / reps
-    t0 = time.perf_counter()
-    k_ref, _ = OP.catalog_cut([b[2] for b in cat], [b[1] for b in cat])
-    ref = OP.pack_fillers(ft, fm, N, rt, rm, 0.0, 180.0)
-    oracle_ms = (time.perf_counter() - t0) * 1e3
     lb = max(max(rt), (sum(rt) + sum(ft)) / N)
     print(json.dumps({"planner": {
         "sequences": len(lengths), "ranks": N, "buckets": len(cat), "k_star": k, "fillers": len(ft),
-        "library_ms": lib_ms, "oracle_ms": oracle_ms, "same_result": bool(k == k_ref and res[0] == ref[0]),
-        "makespan_s": res[4], "lower_bound_s": lb, "makespan_over_lower_bound": res[4] / lb,
-        "overflow": res[3]}}), flush=True)
+        "library_ms": lib_ms, "makespan_s": res[4], "lower_bound_s": lb,
+        "makespan_over_lower_bound": res[4] / lb, "overflow": res[3]}}), flush=True)
 
 
 def main():

@@ -1,7 +1,6 @@
 """Plain Python oracle of the host placement slice (catalog cut, filler packing).
 
-TEST INFRASTRUCTURE ONLY.  Only tests/ and bench.py's planner timing may import this
-module.  It shares no code with the C++ slice and imports nothing from the package.
+TEST INFRASTRUCTURE ONLY.  Only tests/ may import this module.  It shares no code with the C++ slice and imports nothing from the package.
 
 What it computes (method: "Zellige: Moldable Sequence Placement for Mixed Image-Video
 DiT Training"; the pages name both rules without printing them):
