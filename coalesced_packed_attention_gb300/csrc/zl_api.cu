@@ -147,6 +147,7 @@ extern "C" zl_status zl_bwd_main(const zl_plan* p, const void* q, const void* k,
   bp.counter = p->d_counters + kCtrBwd;
   bp.status = p->d_counters + kStatus;
   bp.wait_limit = wait_limit(p);
+  bp.withhold_load = p->test_withhold ? 1 : 0;
   bp.lse = lse;
   bp.ws_d = ws_d;
   bp.ws_dq = ws_d + p->ws_d_floats;

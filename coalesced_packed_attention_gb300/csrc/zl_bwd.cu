@@ -235,9 +235,13 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         ++kt;
         const int kvrow = (int)it.seq_offset + it.kv_lo + tl.block * kBlockN;
         mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(sK + c * L::kBox, &tm_k, kv_full, 64 * c, tl.head, kvrow);
-          tma_load_3d(sV + c * L::kBox, &tm_v, kv_full, 64 * c, tl.head, kvrow);
+        if (p.withhold_load && kt == 1) {
+          // test hook: the announced bytes never arrive; a bounded wait runs out
+        } else {
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d(sK + c * L::kBox, &tm_k, kv_full, 64 * c, tl.head, kvrow);
+            tma_load_3d(sV + c * L::kBox, &tm_v, kv_full, 64 * c, tl.head, kvrow);
+          }
         }
         const int hl = tl.head - it.h_lo;
         for (int is = 0; is < nqb; ++is) {

@@ -29,6 +29,7 @@ struct BwdParams {
   int32_t* counter;
   int32_t* status;
   long long wait_limit;
+  int32_t withhold_load;  // test hook: announce but never issue the first K/V load
   const float* lse;   // final LSE arena
   const float* ws_d;  // row sums D (workspace)
   float* ws_dq;       // fp32 dQ accumulator (workspace, tiled as acc_index)

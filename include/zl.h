@@ -93,9 +93,10 @@ typedef struct zl_plan zl_plan;
 /* Flag for zl_plan_worklist: build the host tables only (no device upload).  Such a
  * plan answers the zl_plan_* queries but cannot be launched. */
 #define ZL_PLAN_HOST_ONLY 1u
-/* Test flag (failure detection): the forward launch announces its first K tile but
- * never issues the copy, so a bounded device wait runs out (after ~20M cycles) and
- * zl_get_device_status reports ZL_ERR_TIMEOUT; nothing faults or hangs. */
+/* Test flag (failure detection): the forward launch announces its first K tile (the
+ * backward launch its first K/V tile) but never issues the copy, so a bounded device
+ * wait runs out (after ~20M cycles) and zl_get_device_status reports ZL_ERR_TIMEOUT;
+ * nothing faults or hangs. */
 #define ZL_PLAN_TEST_WITHHOLD_LOAD 2u
 /* Forward variant: tiles of 128 query rows with one softmax warpgroup per CTA instead
  * of the default 256-row tiles split into two 128-row sub-tiles whose softmax
