@@ -112,14 +112,26 @@ __global__ void __launch_bounds__(256) zl_merge_kernel(const DevGroup* __restric
 #pragma unroll
       for (int s = 16; s > 0; s >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, s);
       lse = m + lg2(tot) * kLn2f;
-      // pass 2: weighted sum of the partial outputs
-      for (int c = 0; c < G.n_members; ++c) {
-        const DevMember mb = members[G.member_begin + c];
-        const float wgt = ex2((__ldg(lse_partial + mb.lse_offset + lse_idx) - lse) * kLog2e);
-        Vec<D> x;
-        x.load(o_partial + mb.o_offset + vec_off);
+      // pass 2: weighted sum of the partial outputs, in member order; up to four
+      // members' rows are loaded before their products are added
+      for (int c0 = 0; c0 < G.n_members; c0 += 4) {
+        Vec<D> x[4];
+        float wgt[4];
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc.v[e] = fmaf(wgt, x.v[e], acc.v[e]);
+        for (int u = 0; u < 4; ++u) {
+          if (c0 + u < G.n_members) {
+            const DevMember mb = members[G.member_begin + c0 + u];
+            wgt[u] = ex2((__ldg(lse_partial + mb.lse_offset + lse_idx) - lse) * kLog2e);
+            x[u].load(o_partial + mb.o_offset + vec_off);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (c0 + u < G.n_members) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc.v[e] = fmaf(wgt[u], x[u].v[e], acc.v[e]);
+          }
+        }
       }
     }
     acc.store_bf16(o + G.out_offset + vec_off);
