@@ -222,7 +222,8 @@ def run_gpu(args):
     t_plan = time.perf_counter()
     plan = zl.zl_plan_worklist(work.items, H, d, T,
                                (zl.ZL_PLAN_FWD_ONE_SUBTILE if args.fwd_one_subtile else 0)
-                               | (zl.ZL_PLAN_FUSE_LOCAL_KMERGE if args.fuse_kmerge else 0))
+                               | (zl.ZL_PLAN_FUSE_LOCAL_KMERGE if args.fuse_kmerge else 0)
+                               | (zl.ZL_PLAN_DETERMINISTIC_DQ if args.deterministic else 0))
     t_plan = time.perf_counter() - t_plan
 
     q, k, v, do_tok = make_inputs(T, H, d, seed=rank, with_grad_output=True, device=str(dev))
@@ -376,7 +377,8 @@ def run_gpu(args):
             "config": {"workload": work.name, "n_heads": H, "head_dim": d, "total_tokens": T,
                        "items": len(work.items), "fwd_tflop": F_fwd / 1e12, "bwd_tflop": F_bwd / 1e12,
                        "l2": "inputs larger than L2 (Q, K, V, dO 302 MB each)",
-                       "parallelism": f"replicas x{ws}", "fused_kmerge": bool(args.fuse_kmerge)},
+                       "parallelism": f"replicas x{ws}", "fused_kmerge": bool(args.fuse_kmerge),
+                       "deterministic_dq": bool(args.deterministic)},
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "stage_ms": {"fwd": fwd_ms, "merge": merge_ms, "bwd_preprocess": pre_ms, "bwd_main": bwd_ms,
                          "bwd_finalize": fin_ms},
@@ -616,6 +618,8 @@ def main():
                     help="time every work item alone and the coalesced list (co-location check)")
     ap.add_argument("--fuse-kmerge", action="store_true",
                     help="plan with ZL_PLAN_FUSE_LOCAL_KMERGE (k-split groups fused into the forward)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="plan with ZL_PLAN_DETERMINISTIC_DQ (ordered, bitwise reproducible dQ adds)")
     ap.add_argument("--kmerge-compare", action="store_true",
                     help="time the long-video forward list merged and fused")
     ap.add_argument("--forward-configs", action="store_true",

@@ -107,7 +107,7 @@ extern "C" zl_status zl_bwd_preprocess(const zl_plan* p, const void* o, const vo
   float* ws_d = static_cast<float*>(workspace);
   cudaError_t e = launch_bwd_pre(p->head_dim, p->d_items, p->n_user, p->total_rowheads,
                                  static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), ws_d,
-                                 ws_d + p->ws_d_floats, p->ws_dq_floats, p->num_sms,
+                                 ws_d + p->ws_d_floats, p->ws_dq_floats + p->ws_turn_ints, p->num_sms,
                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
@@ -151,6 +151,7 @@ extern "C" zl_status zl_bwd_main(const zl_plan* p, const void* q, const void* k,
   bp.lse = lse;
   bp.ws_d = ws_d;
   bp.ws_dq = ws_d + p->ws_d_floats;
+  bp.turns = p->det_dq ? reinterpret_cast<int32_t*>(bp.ws_dq + p->ws_dq_floats) : nullptr;
   bp.dk = dk;
   bp.dv = dv;
   bp.scale = scale;

@@ -29,6 +29,18 @@
 // so they must overlap everything else.  The drain paces its reductions over the
 // block period: issued in a burst they fill each sub-partition's memory-instruction
 // queue and hold up the TMEM loads, MMA issues and TMA issues of the warps beside them.
+// Ordered dQ (plan flag ZL_PLAN_DETERMINISTIC_DQ; a separate instantiation, so the
+// default kernel carries none of it): the order in which CTAs reach a query block
+// decides the order of the fp32 additions, so by default dQ may change in its last bits
+// between runs.  With the flag, each drain warp waits before adding its 32 rows of a
+// block until that slice's turn counter (workspace) equals its KV-block index, and
+// passes the turn on (index + 1, after a fence) when it reaches its next block, by
+// which time most of those reductions have landed (handing it over right after the
+// reductions made the fence wait for all of them: 1.4x slower); every element then
+// sums KV tiles 0, 1, 2, ... in order.  Every tile walks the query blocks from block 0, and the
+// planner lists the tiles of each cost block-major, so the KV tiles of one (item, head)
+// are claimed in ascending order and far apart: waits are rare and only ever on tiles
+// claimed earlier (held by running CTAs), which rules out a cycle of waits.
 // TMEM (512 columns): R0 [0,128) S^T / P^T, R1 [128,256) dP^T / dQ, dV [256,256+d),
 // dK [384,384+d).
 // Warps: 0-7 softmax (two warpgroups), 8-11 dQ drain, 12 TMA producer, 13 MMA issuer,
@@ -102,9 +114,47 @@ __device__ __forceinline__ void red_add_v4(float* addr, uint32_t a, uint32_t b, 
 
 // Tiles of one (item, head) walk the query blocks starting at different blocks, so
 // CTAs running side by side add into different dQ rows instead of contending on one.
+// With ordered dQ adds every tile walks from block 0: a tile then reaches each block no
+// earlier than the tile before it in the add order.
+template <bool kOrdered>
+__device__ __forceinline__ int block_start(int kv_block, int nqb) {
+  if constexpr (kOrdered) return 0;
+  return nqb > 0 ? kv_block % nqb : 0;
+}
 __device__ __forceinline__ int first_block(int step, int start, int n) {
   const int b = start + step;
   return b >= n ? b - n : b;
+}
+
+// Ordered dQ adds (turn counters in global memory, written by other CTAs).
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* a) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int32_t* a, int32_t v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+// Orders this thread's earlier memory operations (the dQ reductions) before its later
+// ones at GPU scope; acquire-release strength is all a turn hand-over needs (a
+// sequentially consistent fence, as __threadfence() issues, costs far more).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Bounded wait until *turn == mine.  The tiles that advance the counter to `mine` were
+// claimed before this one, so they are held by running CTAs; the limit only ends the
+// wait when one of them has given up.
+__device__ __forceinline__ bool wait_turn(const int32_t* turn, int32_t mine, volatile int* abort_flag, long long limit,
+                                          int32_t* status) {
+  if (ld_acquire_gpu(turn) == mine) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    __nanosleep(32);
+    if (ld_acquire_gpu(turn) == mine) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      rec_err(status, abort_flag, ZL_ERR_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // TMEM column of the packed bf16 P^T in R0 for MMA K-step kk (16 queries): queries 0-63
@@ -132,7 +182,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int D>
+template <int D, bool kOrdered>
 __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                         const __grid_constant__ CUtensorMap tm_k,
                                                         const __grid_constant__ CUtensorMap tm_v,
@@ -244,8 +294,9 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           }
         }
         const int hl = tl.head - it.h_lo;
+        const int start = block_start<kOrdered>(tl.block, nqb);
         for (int is = 0; is < nqb; ++is) {
-          const int ib = first_block(is, tl.block % nqb, nqb);
+          const int ib = first_block(is, start, nqb);
           const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
           if (!bwait(q_empty + st, ph ^ 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(q_full + st, L::kTile);
@@ -367,8 +418,13 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
     constexpr int kChunks = D / 32;  // 32-column TMEM loads per row
     constexpr int kReds = kChunks * 8;  // 16-byte reductions per row
     // clock cycles between two reductions of a warp: the previous block period spread
-    // over slightly more than a block's reductions, within these bounds
+    // over slightly more than a block's reductions, within these bounds.  Ordered adds
+    // are not paced: there a block's reductions stand between the turn and the tile
+    // that waits for it, so they go out at once (measured on the training list: 1.15x
+    // faster than pacing at the lower bound, 1.4x faster than pacing by the period,
+    // which includes the turn waits and so slows the successors in turn).
     constexpr long long kPaceMin = 48, kPaceMax = 160;
+    constexpr int kSpread = kReds + kReds / 8;
     const int t = threadIdx.x & 127;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t tile_it = 0, nblocks = 0;
@@ -386,14 +442,29 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
       const int nq = it.q_hi - it.q_lo;
       const int nqb = (nq + kBlockM - 1) / kBlockM;
       float* acc = p.ws_dq + it.ws_dq_offset + (int64_t)(tl.head - it.h_lo) * nqb * (kBlockM * D) + t * 4;
+      // ordered adds: this warp's 32-row slice of accumulator block ib has turn counter
+      // turns[4 (block) + warp slice]; KV tile b adds when the counter reads b.  A
+      // block's turn is passed on at the next block (or the end of the tile), after a
+      // fence that by then mostly finds its reductions complete.
+      auto turn_of = [&](int ib) {
+        return p.turns + 4 * ((acc + (int64_t)ib * (kBlockM * D) - p.ws_dq) / (kBlockM * D)) + (warp & 3);
+      };
+      auto pass_turn = [&](int ib) {
+        fence_acq_rel_gpu();  // this lane's reductions come before the release below
+        __syncwarp();
+        if (lane == 0) st_release_gpu(turn_of(ib), tl.block + 1);
+      };
+      int pending = -1;  // block whose turn this warp still holds
+      const int start = block_start<kOrdered>(tl.block, nqb);
       bool ok = true;
       for (int is = 0; is < nqb; ++is) {
-        const int ib = first_block(is, tl.block % nqb, nqb);
+        const int ib = first_block(is, start, nqb);
         if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
         const long long t_full = clock64();
-        long long pace = t_prev > 0 ? (t_full - t_prev) / (kReds + kReds / 8) : kPaceMin;
+        long long pace = t_prev > 0 ? (t_full - t_prev) / kSpread : kPaceMin;
         pace = pace < kPaceMin ? kPaceMin : (pace > kPaceMax ? kPaceMax : pace);
+        if constexpr (kOrdered) pace = 0;
         t_prev = t_full;
         float* dst = acc + (int64_t)ib * (kBlockM * D);
         const bool row_ok = ib * kBlockM + t < nq;  // rows past the item hold dS = 0
@@ -404,6 +475,14 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(dq_empty);  // the next block's dP^T may overwrite R1
+        if constexpr (kOrdered) {
+          if (pending >= 0) pass_turn(pending);
+          bool mine = true;
+          if (lane == 0) mine = wait_turn(turn_of(ib), tl.block, abort_flag, p.wait_limit, p.status);
+          __syncwarp();  // the other lanes' reductions follow lane 0's acquire
+          if (!__shfl_sync(0xffffffffu, mine ? 1 : 0, 0)) { ok = false; break; }
+          pending = ib;
+        }
         if (row_ok) {
           long long t_next = clock64();
 #pragma unroll
@@ -420,6 +499,9 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         ++nblocks;
       }
       if (!ok) break;
+      if constexpr (kOrdered) {
+        if (pending >= 0) pass_turn(pending);
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -456,7 +538,7 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
       const float* d_row = p.ws_d + it.ws_d_offset + (int64_t)hl * nq;
       bool ok = true;
       float lse_n = -kInfB, d_n = 0.f;  // warpgroup 0 stages -LSE*log2(e) and -D of query t of each block
-      const int ib0 = nqb > 0 ? tl.block % nqb : 0;
+      const int ib0 = block_start<kOrdered>(tl.block, nqb);
       if (wg == 0 && nqb > 0 && ib0 * kBlockM + t < nq) {
         lse_n = -__ldg(lse_row + ib0 * kBlockM + t) * kLog2eB;
         d_n = -__ldg(d_row + ib0 * kBlockM + t);
@@ -593,29 +675,28 @@ cudaError_t launch_bwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& t
                        const BwdParams& p, int num_sms, cudaStream_t stream) {
   const int smem = head_dim == 128 ? BwdLayout<128>::kBytes : BwdLayout<64>::kBytes;
   const int smem_launch = smem > 120 * 1024 ? smem : 120 * 1024;
-  static bool configured[2] = {false, false};
-  const int di = head_dim == 128 ? 1 : 0;
-  if (!configured[di]) {
-    cudaError_t e = head_dim == 128
-                        ? cudaFuncSetAttribute(zl_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_launch)
-                        : cudaFuncSetAttribute(zl_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_launch);
+  using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const BwdParams);
+  const bool ordered = p.turns != nullptr;  // ordered (deterministic) dQ adds
+  const Kernel k = head_dim == 128 ? (ordered ? zl_bwd_kernel<128, true> : zl_bwd_kernel<128, false>)
+                                   : (ordered ? zl_bwd_kernel<64, true> : zl_bwd_kernel<64, false>);
+  static bool configured[2][2] = {{false, false}, {false, false}};
+  const int di = head_dim == 128 ? 1 : 0, oi = ordered ? 1 : 0;
+  if (!configured[di][oi]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_launch);
     if (e != cudaSuccess) return e;
     // the register split adds up to exactly the launch allocation: a kernel built with
     // another per-thread count would leave an increase waiting for registers forever
     cudaFuncAttributes fa;
-    e = head_dim == 128 ? cudaFuncGetAttributes(&fa, zl_bwd_kernel<128>) : cudaFuncGetAttributes(&fa, zl_bwd_kernel<64>);
+    e = cudaFuncGetAttributes(&fa, k);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != (int)kRegsLaunch) return cudaErrorInvalidKernelImage;
-    configured[di] = true;
+    configured[di][oi] = true;
   }
   const int grid = p.n_tiles < num_sms ? p.n_tiles : num_sms;
   if (grid == 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
-  if (head_dim == 128)
-    zl_bwd_kernel<128><<<grid, 512, smem_launch, stream>>>(tq, tk, tv, p);
-  else
-    zl_bwd_kernel<64><<<grid, 512, smem_launch, stream>>>(tq, tk, tv, p);
+  k<<<grid, 512, smem_launch, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

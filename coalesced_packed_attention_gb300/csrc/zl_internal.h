@@ -84,9 +84,11 @@ struct zl_plan {
 
   int64_t o_elems = 0, o_partial_elems = 0, lse_elems = 0, dq_elems = 0, dkv_elems = 0;
   int64_t ws_d_floats = 0, ws_dq_floats = 0, workspace_bytes = 0;
+  int64_t ws_turn_ints = 0;  // dQ turn counters after the accumulator (ZL_PLAN_DETERMINISTIC_DQ)
   int64_t total_rowheads = 0, group_rowheads = 0, merge_rowheads = 0;
   int32_t n_user = 0;        // work-list items; items[n_user..] are fused forward items
   bool fuse_kmerge = false;  // ZL_PLAN_FUSE_LOCAL_KMERGE
+  bool det_dq = false;       // ZL_PLAN_DETERMINISTIC_DQ
 
   // device copies (one allocation, carved)
   void* dev_blob = nullptr;

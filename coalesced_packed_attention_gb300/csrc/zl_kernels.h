@@ -33,6 +33,7 @@ struct BwdParams {
   const float* lse;   // final LSE arena
   const float* ws_d;  // row sums D (workspace)
   float* ws_dq;       // fp32 dQ accumulator (workspace, tiled as acc_index)
+  int32_t* turns;     // deterministic dQ: turn counter per (query block, warp slice); null otherwise
   float* dk;
   float* dv;
   const CUtensorMap* do_maps;  // one per item: its final dO block as [|q|, |h|, d] (device memory)

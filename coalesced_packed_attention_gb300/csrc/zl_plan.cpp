@@ -215,7 +215,9 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
   p->dkv_elems = dkv_next;
   p->ws_d_floats = align_up(wsd_next, 4);
   p->ws_dq_floats = wsq_next;
-  p->workspace_bytes = 4 * (p->ws_d_floats + p->ws_dq_floats);
+  // deterministic dQ: one turn counter per (128-row query block, 32-row warp slice)
+  p->ws_turn_ints = p->det_dq ? 4 * (wsq_next / ((int64_t)kBlockM * d)) : 0;
+  p->workspace_bytes = 4 * (p->ws_d_floats + p->ws_dq_floats + p->ws_turn_ints);
   // ws_dq_offset is relative to the dQ accumulator region, which starts ws_d_floats
   // floats into the workspace (the launchers pass that base pointer)
 
@@ -237,6 +239,9 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
   }
   auto by_cost = [](const DevTile& a, const DevTile& b) { return a.cost > b.cost; };
   std::stable_sort(p->fwd_tiles.begin(), p->fwd_tiles.end(), by_cost);
+  if (p->det_dq)  // block-major within each cost: one head's KV tiles are claimed far apart
+    std::stable_sort(p->bwd_tiles.begin(), p->bwd_tiles.end(),
+                     [](const DevTile& a, const DevTile& b) { return a.block < b.block; });
   std::stable_sort(p->bwd_tiles.begin(), p->bwd_tiles.end(), by_cost);
   if (p->fwd_tiles.size() > (size_t)INT32_MAX || p->bwd_tiles.size() > (size_t)INT32_MAX)
     return ZL_ERR_INVALID_ARG;
@@ -307,7 +312,9 @@ extern "C" zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items
   p->test_withhold = (flags & ZL_PLAN_TEST_WITHHOLD_LOAD) != 0;
   p->fwd_block = (flags & ZL_PLAN_FWD_ONE_SUBTILE) ? kBlockM : kFwdBlockM;
   p->fuse_kmerge = (flags & ZL_PLAN_FUSE_LOCAL_KMERGE) != 0;
+  p->det_dq = (flags & ZL_PLAN_DETERMINISTIC_DQ) != 0;
   zl_status s = build(p, items, n_items);
+  if (s == ZL_OK && p->det_dq) s = zl_plan_check_bounds(p);  // includes the turn order
   if (s == ZL_OK && !p->host_only) s = upload(p);
   if (s != ZL_OK) {
     zl_plan_destroy(p);
@@ -415,7 +422,10 @@ extern "C" zl_status zl_plan_check_bounds(const zl_plan* p) {
       return ZL_ERR_INVALID_ARG;
     if (!in(it.ws_d_offset, nq * nh, p->ws_d_floats) || !in(it.ws_dq_offset, acc_floats(nq, nh, d), p->ws_dq_floats))
       return ZL_ERR_INVALID_ARG;
-    if (4 * (p->ws_d_floats + p->ws_dq_floats) > p->workspace_bytes) return ZL_ERR_INVALID_ARG;
+    if (4 * (p->ws_d_floats + p->ws_dq_floats + p->ws_turn_ints) > p->workspace_bytes) return ZL_ERR_INVALID_ARG;
+    if (p->det_dq && (it.ws_dq_offset % ((int64_t)kBlockM * d) != 0 ||
+                      4 * ((it.ws_dq_offset + acc_floats(nq, nh, d)) / ((int64_t)kBlockM * d)) > p->ws_turn_ints))
+      return ZL_ERR_INVALID_ARG;
   }
   for (size_t g = 0; g < p->groups.size(); ++g) {
     const DevGroup& G = p->groups[g];
@@ -436,11 +446,17 @@ extern "C" zl_status zl_plan_check_bounds(const zl_plan* p) {
     if (t.head < it.h_lo || t.head >= it.h_hi || (int64_t)t.block * p->fwd_block >= it.q_hi - it.q_lo)
       return ZL_ERR_INVALID_ARG;
   }
+  // deterministic dQ: the KV tiles of each (item, head) must be claimed in the order of
+  // their turns (0, 1, 2, ...), so that a tile only ever waits on tiles claimed before it
+  std::vector<int64_t> head_base(p->n_user + 1, 0);
+  for (int32_t i = 0; i < p->n_user; ++i) head_base[i + 1] = head_base[i] + (p->items[i].h_hi - p->items[i].h_lo);
+  std::vector<int32_t> next_turn(p->det_dq ? head_base[p->n_user] : 0, 0);
   for (const auto& t : p->bwd_tiles) {
     if (t.item < 0 || t.item >= p->n_user) return ZL_ERR_INVALID_ARG;
     const DevItem& it = p->items[t.item];
     if (t.head < it.h_lo || t.head >= it.h_hi || (int64_t)t.block * kBlockN >= it.kv_hi - it.kv_lo)
       return ZL_ERR_INVALID_ARG;
+    if (p->det_dq && next_turn[head_base[t.item] + t.head - it.h_lo]++ != t.block) return ZL_ERR_INVALID_ARG;
   }
   return ZL_OK;
 }

@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(256) zl_bwd_pre_kernel(const DevItem* __restri
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  // zero the whole accumulator (a multiple of 4 floats, 16-byte aligned)
+  // zero the whole accumulator and any turn counters after it (a multiple of 4
+  // words, 16-byte aligned)
   {
     float4* z4 = reinterpret_cast<float4*>(ws_dq);
     const int64_t n4 = acc_total / 4, nthreads = (int64_t)gridDim.x * blockDim.x;

@@ -20,6 +20,7 @@ ZL_PLAN_HOST_ONLY = 1
 ZL_PLAN_TEST_WITHHOLD_LOAD = 2
 ZL_PLAN_FWD_ONE_SUBTILE = 4
 ZL_PLAN_FUSE_LOCAL_KMERGE = 8
+ZL_PLAN_DETERMINISTIC_DQ = 16
 
 
 class ZlError(RuntimeError):

@@ -114,6 +114,20 @@ typedef struct zl_plan zl_plan;
  * usual.  The backward is unchanged: each member keeps its gradient ownership and reads
  * the group's final O and LSE. */
 #define ZL_PLAN_FUSE_LOCAL_KMERGE 8u
+/* Deterministic dQ.  By default the backward's CTAs add their dQ contributions into the
+ * fp32 accumulator in whatever order they reach a query block, so dQ may differ in its
+ * last bits from run to run (dK, dV, O and LSE never do).  With this flag every
+ * accumulator element receives its contributions in a fixed order, KV tile 0, 1, 2, ...
+ * of its item and head, so dQ is bitwise reproducible for the same plan and inputs.
+ * How: each drain warp of a KV tile waits (bounded) until a per-(query block, warp)
+ * turn counter equals the tile's KV-block index, adds its rows, and passes the turn on
+ * (index + 1) when it moves to its next block.
+ * The backward tiles of each cost are listed block-major (KV block, then work-list
+ * order), so the tiles of one item and head are claimed in ascending KV order and far
+ * apart: a tile waits only on tiles claimed before it, held by running CTAs, and
+ * rarely at all.  The workspace grows by one int32 per (128-row query block, 32-row
+ * warp slice) of the accumulator, zeroed with it by zl_bwd_preprocess. */
+#define ZL_PLAN_DETERMINISTIC_DQ 16u
 
 /* Validate a work list and build its tile lists (host C++), then upload them to the
  * current device.
@@ -138,8 +152,8 @@ ZL_API zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items, in
 ZL_API void zl_plan_destroy(zl_plan* plan);
 
 /* Element counts of every arena the caller must allocate for this plan (any pointer
- * may be NULL).  workspace_bytes: scratch for zl_coalesced_attn_bwd (row sums D and
- * the fp32 dQ accumulator). */
+ * may be NULL).  workspace_bytes: scratch for zl_coalesced_attn_bwd (row sums D, the
+ * fp32 dQ accumulator and, with ZL_PLAN_DETERMINISTIC_DQ, its turn counters). */
 ZL_API zl_status zl_plan_arena_sizes(const zl_plan* plan, int64_t* o_elems, int64_t* o_partial_elems,
                               int64_t* lse_elems, int64_t* dq_elems, int64_t* dkv_elems,
                               int64_t* workspace_bytes);
@@ -215,7 +229,8 @@ ZL_API zl_status zl_coalesced_attn_bwd(const zl_plan* plan, const void* q, const
 /* The three launches of zl_coalesced_attn_bwd, callable one by one (same arguments,
  * same order of use); zl_coalesced_attn_bwd is exactly these three in sequence.
  *   zl_bwd_preprocess: D_i = rowsum(dO_i * O_i) into the workspace and zeroing of the
- *     workspace's fp32 dQ accumulator (HBM-bound, one warp per (row, head)).
+ *     workspace's fp32 dQ accumulator (and turn counters) (HBM-bound, one warp per
+ *     (row, head)).
  *   zl_bwd_main: the persistent tcgen05 backward over (item, head, 128 KV rows) tiles;
  *     writes dk, dv and accumulates unscaled dQ in the workspace.
  *   zl_bwd_finalize: dq = scale * accumulator, per item block. */

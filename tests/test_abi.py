@@ -169,16 +169,46 @@ def _all_lists():
     return lists
 
 
-@pytest.mark.parametrize("flags", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE, zl.ZL_PLAN_FUSE_LOCAL_KMERGE])
+@pytest.mark.parametrize("flags", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE, zl.ZL_PLAN_FUSE_LOCAL_KMERGE,
+                                   zl.ZL_PLAN_DETERMINISTIC_DQ,
+                                   zl.ZL_PLAN_DETERMINISTIC_DQ | zl.ZL_PLAN_FUSE_LOCAL_KMERGE])
 def test_every_plan_passes_the_bounds_dry_run(flags):
     for w in _all_lists():
         p = zl.zl_plan_worklist(w.items, w.n_heads, w.head_dim, w.total_tokens,
                                 flags=zl.ZL_PLAN_HOST_ONLY | flags)
         p.check_bounds()
         # the workspace holds D ([|h|,|q|] fp32) and the dQ accumulator (fp32, |q| padded
-        # to whole 128-row query blocks) for every item, and nothing else
+        # to whole 128-row query blocks) for every item, plus with ordered dQ adds one
+        # int32 turn counter per 32 rows of the accumulator, and nothing else
         need = sum(4 * it.nh * (it.nq + -(-it.nq // 128) * 128 * w.head_dim) for it in w.items)
+        if flags & zl.ZL_PLAN_DETERMINISTIC_DQ:
+            need += sum(16 * it.nh * -(-it.nq // 128) for it in w.items)
         assert need <= p.workspace_bytes <= need + 16
+
+
+@pytest.mark.parametrize("make", [config_tiny, config_images, config_mixed, config_long_video])
+def test_deterministic_dq_plan_claims_each_heads_kv_tiles_in_order(make):
+    # ZL_PLAN_DETERMINISTIC_DQ: the same backward tiles, longest first, but block-major
+    # within each cost, so the KV tiles of one (item, head) are claimed in ascending
+    # order (a tile's turn comes after every tile it waits on) and far apart
+    w = make()
+    base = host_plan(w)
+    p = zl.zl_plan_worklist(w.items, w.n_heads, w.head_dim, w.total_tokens,
+                            flags=zl.ZL_PLAN_HOST_ONLY | zl.ZL_PLAN_DETERMINISTIC_DQ)
+    tiles = p.tiles(1)
+    assert sorted(tiles) == sorted(base.tiles(1))
+    assert p.tiles(0) == base.tiles(0)
+    costs = [t[3] for t in tiles]
+    assert costs == sorted(costs, reverse=True)
+    for a, b in zip(tiles, tiles[1:]):
+        if a[3] == b[3]:
+            assert (a[2], a[0], a[1]) < (b[2], b[0], b[1])
+    next_turn = {}
+    for (i, h, b, _) in tiles:
+        assert next_turn.get((i, h), 0) == b
+        next_turn[(i, h)] = b + 1
+    blocks = sum(it.nh * -(-it.nq // 128) for it in w.items)
+    assert p.workspace_bytes == base.workspace_bytes + 16 * blocks
 
 
 def _union(items):
