@@ -679,22 +679,22 @@ cudaError_t launch_bwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& t
   const bool ordered = p.turns != nullptr;  // ordered (deterministic) dQ adds
   const Kernel k = head_dim == 128 ? (ordered ? zl_bwd_kernel<128, true> : zl_bwd_kernel<128, false>)
                                    : (ordered ? zl_bwd_kernel<64, true> : zl_bwd_kernel<64, false>);
-  static bool configured[2][2] = {{false, false}, {false, false}};
+  static PerDeviceOnce configured[2][2];
   const int di = head_dim == 128 ? 1 : 0, oi = ordered ? 1 : 0;
-  if (!configured[di][oi]) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_launch);
-    if (e != cudaSuccess) return e;
+  cudaError_t e = configured[di][oi].run([&] {
+    cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_launch);
+    if (r != cudaSuccess) return r;
     // the register split adds up to exactly the launch allocation: a kernel built with
     // another per-thread count would leave an increase waiting for registers forever
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, k);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != (int)kRegsLaunch) return cudaErrorInvalidKernelImage;
-    configured[di][oi] = true;
-  }
+    r = cudaFuncGetAttributes(&fa, k);
+    if (r != cudaSuccess) return r;
+    return fa.numRegs == (int)kRegsLaunch ? cudaSuccess : cudaErrorInvalidKernelImage;
+  });
+  if (e != cudaSuccess) return e;
   const int grid = p.n_tiles < num_sms ? p.n_tiles : num_sms;
   if (grid == 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream);
+  e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
   k<<<grid, 512, smem_launch, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

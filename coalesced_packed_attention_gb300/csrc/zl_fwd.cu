@@ -415,15 +415,13 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const FwdParams& p, int num_sms, cudaStream_t stream) {
   using L = FwdLayout<D>;
   const int smem = L::kAlloc > 120 * 1024 ? L::kAlloc : 120 * 1024;  // one CTA per SM (TMEM 512 cols)
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(zl_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce configured;
+  cudaError_t e = configured.run(
+      [&] { return cudaFuncSetAttribute(zl_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
+  if (e != cudaSuccess) return e;
   const int grid = p.n_tiles < num_sms ? p.n_tiles : num_sms;
   if (grid == 0) return cudaSuccess;
-  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream);
+  e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return e;
   zl_fwd_kernel<D><<<grid, 192, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <vector>
 
 #include "../../include/zl.h"
@@ -56,6 +57,28 @@ struct DevGroup {          // one k-split merge group
 struct DevMember {         // one partial of a merge group
   int64_t o_offset;        // [nq, nh, d] block in o_partial
   int64_t lse_offset;      // [nh, nq] block in lse_partial
+};
+
+// Once-per-device setup of a kernel's launch attributes.  cudaFuncSetAttribute acts on
+// the current device, so a process that drives several GPUs must set them on each; two
+// host threads may both run the setup, which is harmless (it is idempotent).
+class PerDeviceOnce {
+ public:
+  template <typename F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return setup();  // outside the mask: set up every time
+    const uint64_t bit = 1ull << dev;
+    if (done_.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess) done_.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+  }
+
+ private:
+  std::atomic<uint64_t> done_{0};
 };
 
 // Scheduler counters and the status word live in one small device block.
