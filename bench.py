@@ -101,14 +101,22 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def kernel_source_sha256(kernel: str) -> str:
+    """Hash of a kernel's device code: its source file up to the host launcher (the
+    first `cudaError_t launch_` definition), so that a host-only change to the launch
+    does not void counters taken on the kernel."""
+    text = open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb").read()
+    cut = text.find(b"\ncudaError_t launch_")
+    return hashlib.sha256(text[:cut] if cut > 0 else text).hexdigest()
+
+
 def recorded_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current source of that kernel (else None)."""
+    current device code of that kernel (else None)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_training_traffic.txt")
-    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
     if not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    sha = kernel_source_sha256(kernel)
     vals = {}
     for ln in open(path):
         if ":" in ln:
@@ -355,13 +363,14 @@ def run_gpu(args):
     peaks, peak_kind = measured_peaks()
     med = np.median(parts, axis=0)
     fwd_ms, merge_ms, pre_ms, bwd_ms, fin_ms = (float(x) for x in med)
+    step_each = parts.sum(axis=1)  # device time of each timed step (its five stages)
     # dominant kernel: the tcgen05 backward (largest share of the step)
     bwd_tf = F_bwd / (bwd_ms * 1e-3) / 1e12
     fwd_tf = F_fwd / (fwd_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops_sustained"])
     traffic = recorded_traffic("zl_bwd_main")
     # algorithmic bytes of the HBM-bound kernels
-    merge_bytes = sum(8 * 0 for _ in [])  # filled below
+    merge_bytes = 0
     grp_rows = 0
     for g in range(plan.n_groups):
         members, _, _ = plan.group(g)
@@ -382,6 +391,8 @@ def run_gpu(args):
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "stage_ms": {"fwd": fwd_ms, "merge": merge_ms, "bwd_preprocess": pre_ms, "bwd_main": bwd_ms,
                          "bwd_finalize": fin_ms},
+            "step_ms": {"median": float(np.median(step_each)), "min": float(step_each.min()),
+                        "max": float(step_each.max())},
             "merge_gbs": merge_bytes / (merge_ms * 1e-3) / 1e9 if merge_ms > 0 and plan.n_merge_groups else None,
             "bwd_preprocess_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9 if pre_ms > 0 else None,
             "plan_ms": t_plan * 1e3,
