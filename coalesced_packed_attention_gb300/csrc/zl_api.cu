@@ -47,7 +47,13 @@ bool make_block_map(CUtensorMap* m, const void* base, int64_t rows, int32_t H, i
   return make_qkv_map(m, base, rows, H, d);
 }
 
-bool launchable(const zl_plan* p) { return p && !p->host_only && p->d_items; }
+// A plan that can be launched, with the device it was built on current: its tile lists,
+// counters and status word live in that device's memory.
+bool launchable(const zl_plan* p) {
+  if (!p || p->host_only || !p->d_items) return false;
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess && dev == p->device;
+}
 
 // Spin budget of a bounded device wait: ~0.5 s at 2 GHz; short for the test hook.
 long long wait_limit(const zl_plan* p) { return p->test_withhold ? 20000000LL : 1000000000LL; }

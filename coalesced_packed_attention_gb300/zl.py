@@ -109,9 +109,11 @@ class ItemPlacement:
 class Plan:
     """Owner of one zl_plan*.  Created by zl_plan_worklist()."""
 
-    def __init__(self, handle: int, n_heads: int, head_dim: int, total_tokens: int, host_only: bool):
+    def __init__(self, handle: int, n_heads: int, head_dim: int, total_tokens: int, host_only: bool,
+                 device: Optional[int] = None):
         self.handle = ctypes.c_void_p(handle)
         self.n_heads, self.head_dim, self.total_tokens, self.host_only = n_heads, head_dim, total_tokens, host_only
+        self.device = device  # CUDA device index the plan was built on (None: host-only plan)
         L = load_library()
         v = [ctypes.c_int64() for _ in range(6)]
         _check(L.zl_plan_arena_sizes(self.handle, *[ctypes.byref(x) for x in v]), "zl_plan_arena_sizes")
@@ -148,12 +150,17 @@ class Plan:
         return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
 
     def group(self, g: int):
+        """(member item ids, final O offset, final LSE offset) of merge group g."""
         n = ctypes.c_int32()
         oo, lo = ctypes.c_int64(), ctypes.c_int64()
-        buf = (ctypes.c_int32 * 1024)()
-        _check(load_library().zl_plan_group(self.handle, g, buf, 1024, ctypes.byref(n), ctypes.byref(oo),
-                                            ctypes.byref(lo)), "zl_plan_group")
-        return list(buf[:n.value]), oo.value, lo.value
+        cap = 64
+        while True:
+            buf = (ctypes.c_int32 * cap)()
+            _check(load_library().zl_plan_group(self.handle, g, buf, cap, ctypes.byref(n), ctypes.byref(oo),
+                                                ctypes.byref(lo)), "zl_plan_group")
+            if n.value <= cap:
+                return list(buf[:n.value]), oo.value, lo.value
+            cap = n.value
 
     def destroy(self):
         if self.handle is not None and self.handle.value:
@@ -178,9 +185,15 @@ def _to_c_items(items: Sequence) -> ctypes.Array:
 def zl_plan_worklist(items: Sequence, n_heads: int, head_dim: int, total_tokens: int, flags: int = 0) -> Plan:
     L = load_library()
     h = ctypes.c_void_p()
+    host_only = bool(flags & ZL_PLAN_HOST_ONLY)
+    device = None
+    if not host_only:
+        import torch
+        if torch.cuda.is_available():  # else the library reports the missing device
+            device = torch.cuda.current_device()
     _check(L.zl_plan_worklist(_to_c_items(items), len(items), n_heads, head_dim, total_tokens, flags,
                               ctypes.byref(h)), "zl_plan_worklist")
-    return Plan(h.value, n_heads, head_dim, total_tokens, bool(flags & ZL_PLAN_HOST_ONLY))
+    return Plan(h.value, n_heads, head_dim, total_tokens, host_only, device)
 
 
 # ---------------------------------------------------------------- launches
@@ -197,6 +210,14 @@ def _ptr(t, dtype, what, numel=None):
     if numel is not None and t.numel() < numel:
         raise ValueError(f"{what}: needs at least {numel} elements, has {t.numel()}")
     return t.data_ptr()
+
+
+def _on_plan_device(plan: Plan, *tensors):
+    """Every tensor lives on the plan's device (the library checks the current device)."""
+    for t in tensors:
+        if t is not None and getattr(t, "device", None) is not None and t.device.type == "cuda" \
+                and t.device.index != plan.device:
+            raise ValueError(f"tensor on cuda:{t.device.index}, plan built on cuda:{plan.device}")
 
 
 def _stream(stream):
@@ -217,6 +238,7 @@ def _qkv(plan: Plan, q, k, v):
 
 def zl_coalesced_attn_fwd(plan: Plan, q, k, v, o, o_partial, lse, scale: float, stream=None):
     import torch
+    _on_plan_device(plan, q, k, v, o, o_partial, lse)
     pq, pk, pv = _qkv(plan, q, k, v)
     st = load_library().zl_coalesced_attn_fwd(
         plan.handle, pq, pk, pv,
@@ -228,6 +250,7 @@ def zl_coalesced_attn_fwd(plan: Plan, q, k, v, o, o_partial, lse, scale: float, 
 
 def zl_merge_partials(plan: Plan, o_partial, lse_partial, o, lse_out, stream=None):
     import torch
+    _on_plan_device(plan, o_partial, lse_partial, o, lse_out)
     st = load_library().zl_merge_partials(
         plan.handle, _ptr(o_partial, torch.float32, "o_partial", plan.o_partial_elems),
         _ptr(lse_partial, torch.float32, "lse_partial", plan.lse_elems),
@@ -238,6 +261,7 @@ def zl_merge_partials(plan: Plan, o_partial, lse_partial, o, lse_out, stream=Non
 
 def zl_coalesced_attn_bwd(plan: Plan, q, k, v, o, d_o, lse, dq, dk, dv, workspace, scale: float, stream=None):
     import torch
+    _on_plan_device(plan, q, k, v, o, d_o, lse, dq, dk, dv, workspace)
     pq, pk, pv = _qkv(plan, q, k, v)
     st = load_library().zl_coalesced_attn_bwd(
         plan.handle, pq, pk, pv, _ptr(o, torch.bfloat16, "o", plan.o_elems),
@@ -250,6 +274,7 @@ def zl_coalesced_attn_bwd(plan: Plan, q, k, v, o, d_o, lse, dq, dk, dv, workspac
 
 def zl_bwd_preprocess(plan: Plan, o, d_o, workspace, stream=None):
     import torch
+    _on_plan_device(plan, o, d_o, workspace)
     _check(load_library().zl_bwd_preprocess(
         plan.handle, _ptr(o, torch.bfloat16, "o", plan.o_elems), _ptr(d_o, torch.bfloat16, "d_o", plan.o_elems),
         _ptr(workspace, torch.uint8, "workspace", plan.workspace_bytes), _stream(stream)), "zl_bwd_preprocess")
@@ -257,6 +282,7 @@ def zl_bwd_preprocess(plan: Plan, o, d_o, workspace, stream=None):
 
 def zl_bwd_main(plan: Plan, q, k, v, d_o, lse, dk, dv, workspace, scale: float, stream=None):
     import torch
+    _on_plan_device(plan, q, k, v, d_o, lse, dk, dv, workspace)
     pq, pk, pv = _qkv(plan, q, k, v)
     _check(load_library().zl_bwd_main(
         plan.handle, pq, pk, pv, _ptr(d_o, torch.bfloat16, "d_o", plan.o_elems),
@@ -267,6 +293,7 @@ def zl_bwd_main(plan: Plan, q, k, v, d_o, lse, dk, dv, workspace, scale: float, 
 
 def zl_bwd_finalize(plan: Plan, dq, workspace, scale: float, stream=None):
     import torch
+    _on_plan_device(plan, dq, workspace)
     _check(load_library().zl_bwd_finalize(
         plan.handle, _ptr(dq, torch.float32, "dq", plan.dq_elems),
         _ptr(workspace, torch.uint8, "workspace", plan.workspace_bytes), ctypes.c_float(scale), _stream(stream)),

@@ -29,7 +29,8 @@
  *    ordered by events).
  *  - No call throws; every call returns a zl_status.  A launch error is ZL_ERR_CUDA
  *    and leaves the CUDA error state for the caller to inspect.
- *  - Plans are bound to the device that was current when zl_plan_worklist ran.
+ *  - Plans are bound to the device that was current when zl_plan_worklist ran; a launch
+ *    or status query with another device current returns ZL_ERR_INVALID_ARG.
  *
  * Output arenas (element offsets; the planner assigns every offset left at -1)
  *  - o (bf16): one [|q|, |h|, d] block per non-k-split item and per merge group.  An
