@@ -63,9 +63,7 @@ long long wait_limit(const zl_plan* p) { return p->test_withhold ? 20000000LL : 
 extern "C" zl_status zl_coalesced_attn_fwd(const zl_plan* p, const void* q, const void* k, const void* v, void* o,
                                            float* o_partial, float* lse, float scale, void* stream) {
   if (!launchable(p) || !q || !k || !v || !lse) return ZL_ERR_INVALID_ARG;
-  bool any_whole = false, any_emit = false;
-  for (const auto& t : p->fwd_tiles) (p->items[t.item].emit_lse ? any_emit : any_whole) = true;
-  if ((any_whole && !o) || (any_emit && !o_partial)) return ZL_ERR_INVALID_ARG;
+  if ((p->fwd_writes_o && !o) || (p->fwd_writes_partial && !o_partial)) return ZL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(o_partial) ||
       !aligned16(lse))
     return ZL_ERR_ALIGN;

@@ -112,6 +112,7 @@ struct zl_plan {
   int32_t n_user = 0;        // work-list items; items[n_user..] are fused forward items
   bool fuse_kmerge = false;  // ZL_PLAN_FUSE_LOCAL_KMERGE
   bool det_dq = false;       // ZL_PLAN_DETERMINISTIC_DQ
+  bool fwd_writes_o = false, fwd_writes_partial = false;  // some forward tile writes o / o_partial
 
   // device copies (one allocation, carved)
   void* dev_blob = nullptr;

@@ -245,6 +245,7 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
   std::stable_sort(p->bwd_tiles.begin(), p->bwd_tiles.end(), by_cost);
   if (p->fwd_tiles.size() > (size_t)INT32_MAX || p->bwd_tiles.size() > (size_t)INT32_MAX)
     return ZL_ERR_INVALID_ARG;
+  for (const auto& t : p->fwd_tiles) (p->items[t.item].emit_lse ? p->fwd_writes_partial : p->fwd_writes_o) = true;
   return ZL_OK;
 }
 
