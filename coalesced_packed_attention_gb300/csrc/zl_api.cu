@@ -62,6 +62,7 @@ long long wait_limit(const zl_plan* p) { return p->test_withhold ? 20000000LL : 
 
 extern "C" zl_status zl_coalesced_attn_fwd(const zl_plan* p, const void* q, const void* k, const void* v, void* o,
                                            float* o_partial, float* lse, float scale, void* stream) {
+  NvtxRange range("zl_coalesced_attn_fwd");
   if (!launchable(p) || !q || !k || !v || !lse) return ZL_ERR_INVALID_ARG;
   if ((p->fwd_writes_o && !o) || (p->fwd_writes_partial && !o_partial)) return ZL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(o_partial) ||
@@ -93,6 +94,7 @@ extern "C" zl_status zl_coalesced_attn_fwd(const zl_plan* p, const void* q, cons
 
 extern "C" zl_status zl_merge_partials(const zl_plan* p, const float* o_partial, const float* lse_partial, void* o,
                                        float* lse_out, void* stream) {
+  NvtxRange range("zl_merge_partials");
   if (!launchable(p)) return ZL_ERR_INVALID_ARG;
   if (p->merge_groups.empty()) return ZL_OK;  // none, or all fused into the forward
   if (!o_partial || !lse_partial || !o || !lse_out) return ZL_ERR_INVALID_ARG;
@@ -105,6 +107,7 @@ extern "C" zl_status zl_merge_partials(const zl_plan* p, const float* o_partial,
 
 extern "C" zl_status zl_bwd_preprocess(const zl_plan* p, const void* o, const void* d_o, void* workspace,
                                        void* stream) {
+  NvtxRange range("zl_bwd_preprocess");
   if (!launchable(p) || !o || !d_o || (p->workspace_bytes > 0 && !workspace)) return ZL_ERR_INVALID_ARG;
   if (!aligned16(o) || !aligned16(d_o) || !aligned16(workspace)) return ZL_ERR_ALIGN;
   if (p->items.empty()) return ZL_OK;
@@ -118,6 +121,7 @@ extern "C" zl_status zl_bwd_preprocess(const zl_plan* p, const void* o, const vo
 
 extern "C" zl_status zl_bwd_main(const zl_plan* p, const void* q, const void* k, const void* v, const void* d_o,
                                  const float* lse, float* dk, float* dv, void* workspace, float scale, void* stream) {
+  NvtxRange range("zl_bwd_main");
   if (!launchable(p) || !q || !k || !v || !d_o || !lse || !dk || !dv || (p->workspace_bytes > 0 && !workspace))
     return ZL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) || !aligned16(lse) || !aligned16(dk) ||
@@ -166,6 +170,7 @@ extern "C" zl_status zl_bwd_main(const zl_plan* p, const void* q, const void* k,
 }
 
 extern "C" zl_status zl_bwd_finalize(const zl_plan* p, float* dq, void* workspace, float scale, void* stream) {
+  NvtxRange range("zl_bwd_finalize");
   if (!launchable(p) || !dq || (p->workspace_bytes > 0 && !workspace)) return ZL_ERR_INVALID_ARG;
   if (!aligned16(dq) || !aligned16(workspace)) return ZL_ERR_ALIGN;
   if (p->items.empty()) return ZL_OK;
@@ -178,6 +183,7 @@ extern "C" zl_status zl_bwd_finalize(const zl_plan* p, float* dq, void* workspac
 extern "C" zl_status zl_coalesced_attn_bwd(const zl_plan* p, const void* q, const void* k, const void* v,
                                            const void* o, const void* d_o, const float* lse, float* dq, float* dk,
                                            float* dv, void* workspace, float scale, void* stream) {
+  NvtxRange range("zl_coalesced_attn_bwd");
   if (!launchable(p) || !q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv ||
       (p->workspace_bytes > 0 && !workspace))
     return ZL_ERR_INVALID_ARG;

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 #include <vector>
 
@@ -57,6 +59,17 @@ struct DevGroup {          // one k-split merge group
 struct DevMember {         // one partial of a merge group
   int64_t o_offset;        // [nq, nh, d] block in o_partial
   int64_t lse_offset;      // [nh, nq] block in lse_partial
+};
+
+// Named NVTX range over one ABI call (host side: it covers validation and the enqueue of
+// the launches), so timelines and ncu's NVTX filters can find each call.  A no-op
+// unless a profiling tool is attached.
+class NvtxRange {
+ public:
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
 // Once-per-device setup of a kernel's launch attributes.  cudaFuncSetAttribute acts on

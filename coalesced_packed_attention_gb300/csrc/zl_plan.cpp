@@ -298,6 +298,7 @@ zl_status upload(zl_plan* p) {
 extern "C" zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items, int32_t n_heads,
                                       int32_t head_dim, int64_t total_tokens, uint32_t flags,
                                       zl_plan** out) {
+  NvtxRange range("zl_plan_worklist");
   if (!out) return ZL_ERR_INVALID_ARG;
   *out = nullptr;
   if (n_items < 0 || (n_items > 0 && !items) || n_heads < 1 || total_tokens < 1 ||
