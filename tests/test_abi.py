@@ -274,3 +274,26 @@ def test_fused_local_kmerge_leaves_gapped_groups():
     p = zl.zl_plan_worklist(items, 2, 64, 300, flags=zl.ZL_PLAN_HOST_ONLY | zl.ZL_PLAN_FUSE_LOCAL_KMERGE)
     assert p.n_merge_groups == 1 and all(p.item(i).item.out_offset >= 0 for i in range(2))
     p.check_bounds()
+
+
+def test_group_of_many_members_is_read_whole():
+    # 100 k-chunks of one sequence form one merge group; the binding reads all of them
+    items = [WorkItem(0, 1000, 0, 1000, 0, 2, 10 * c, 10 * c + 10, 1) for c in range(100)]
+    p = zl.zl_plan_worklist(items, 2, 64, 1000, flags=zl.ZL_PLAN_HOST_ONLY)
+    assert p.n_groups == 1
+    members, _, _ = p.group(0)
+    assert members == list(range(100))
+
+
+def test_tensors_on_another_device_are_rejected_before_the_call():
+    import torch
+
+    class Fake:  # stands in for a tensor: only its device is looked at
+        def __init__(self, index):
+            self.device = torch.device("cuda", index)
+
+    p = zl.zl_plan_worklist(config_tiny().items, 4, 64, config_tiny().total_tokens, flags=zl.ZL_PLAN_HOST_ONLY)
+    p.device = 0
+    zl._on_plan_device(p, Fake(0), None, Fake(0))
+    with pytest.raises(ValueError):
+        zl._on_plan_device(p, Fake(0), Fake(1))
