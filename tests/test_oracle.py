@@ -4,7 +4,7 @@ Each test would catch a plausible mistake in the oracle: a dropped term, a wrong
 a wrong index or a transposed operand.  Sources:
   * brute force (scalar Python loops) on tiny inputs,
   * closed forms (single key, zero query, constant values, one dominant logit,
-    a hand-worked example in tests/golden/worked_example.json),
+    hand-worked examples in tests/golden/ with score scales 1 and 2),
   * invariants (rows of P sum to 1, merge of any k split equals the unsplit result,
     q and h shards tile the whole output, KV permutation invariance,
     sum_j dS_ij = 0),
@@ -60,8 +60,9 @@ def test_forward_matches_brute_force_tiny_mixed():
 
 
 # ---------------------------------------------------------------- closed forms
-def test_golden_worked_example():
-    with open(os.path.join(GOLDEN, "worked_example.json")) as f:
+@pytest.mark.parametrize("name", ["worked_example.json", "worked_example_scale2.json"])
+def test_golden_worked_example(name):
+    with open(os.path.join(GOLDEN, name)) as f:
         g = json.load(f)
     ns = {"e": math.e, "log": math.log, "exp": math.exp}
     ev = lambda a: np.array([[eval(x, {}, ns) for x in r] for r in a])  # noqa: E731
