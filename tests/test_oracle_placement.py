@@ -58,8 +58,16 @@ def test_cut_invariances():
 def test_pack_single_rank_and_one_each():
     a, L, M, over, mk = P.pack_fillers([3.0, 1.0, 2.0], [1.0, 1.0, 1.0], 1, M_cap=10.0)
     assert a == [0, 0, 0] and mk == 6.0 and over == 0
+    # equal fillers on empty ranks: each goes to the lowest of the equally open ranks
     a, L, M, over, mk = P.pack_fillers([2.0] * 4, [0.5] * 4, 4, M_cap=1.0)
-    assert sorted(a) == [0, 1, 2, 3] and L == [2.0] * 4 and over == 0
+    assert a == [0, 1, 2, 3] and L == [2.0] * 4 and over == 0
+
+
+def test_pack_places_longest_first():
+    # 1, 1, 1, 1, 4 on two ranks: longest first puts the 4 alone and reaches the optimum
+    # 4; shortest first would end at 6
+    a, L, M, over, mk = P.pack_fillers([1.0, 1.0, 1.0, 1.0, 4.0], [0.0] * 5, 2, M_cap=1.0)
+    assert mk == 4.0 and a[4] == 0 and a[:4] == [1, 1, 1, 1]
 
 
 def test_pack_memory_binds():
