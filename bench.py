@@ -133,15 +133,8 @@ def recorded_traffic(kernel: str):
 def dO_arena(plan, work, do_tok, device):
     """dO laid out like the `o` arena: each item's final block gets the matching rows and
     heads of the [T, H, d] gradient."""
-    import torch
-    d = work.head_dim
-    arena = torch.zeros(max(plan.o_elems, 8), dtype=torch.bfloat16, device=device)
-    for i, it in enumerate(work.items):
-        pl = plan.item(i)
-        n = it.nq * it.nh * d
-        arena[pl.fin_out_offset: pl.fin_out_offset + n] = \
-            do_tok[it.seq_offset + it.q_lo: it.seq_offset + it.q_hi, it.h_lo:it.h_hi].reshape(-1)
-    return arena
+    from coalesced_packed_attention_gb300 import zl
+    return zl.o_arena_from_tokens(plan, work.items, do_tok.to(device))
 
 
 def oracle_inputs(work, seed=0):

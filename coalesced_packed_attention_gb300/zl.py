@@ -324,6 +324,21 @@ def allocate(plan: Plan, device="cuda", backward: bool = False) -> Dict[str, "ob
     return out
 
 
+def o_arena_from_tokens(plan: Plan, items: Sequence, x):
+    """A [T, H, d] token tensor laid out like the `o` arena: each work item's final block
+    (its own, or its merge group's) holds that item's query rows and heads of x.  This is
+    the layout in which the backward reads the output gradient dO."""
+    import torch
+    d = plan.head_dim
+    arena = torch.zeros(max(plan.o_elems, 8), dtype=x.dtype, device=x.device)
+    for i, it in enumerate(items):
+        pl = plan.item(i)
+        n = (it.q_hi - it.q_lo) * (it.h_hi - it.h_lo) * d
+        arena[pl.fin_out_offset: pl.fin_out_offset + n] = \
+            x[it.seq_offset + it.q_lo: it.seq_offset + it.q_hi, it.h_lo:it.h_hi].reshape(-1)
+    return arena
+
+
 def forward(plan: Plan, q, k, v, scale: float, bufs: Optional[dict] = None, stream=None) -> dict:
     """Forward of every item, then the merge of every k-split group."""
     bufs = bufs if bufs is not None else allocate(plan, q.device)

@@ -297,3 +297,25 @@ def test_tensors_on_another_device_are_rejected_before_the_call():
     zl._on_plan_device(p, Fake(0), None, Fake(0))
     with pytest.raises(ValueError):
         zl._on_plan_device(p, Fake(0), Fake(1))
+
+
+@pytest.mark.parametrize("make", [config_tiny, config_mixed])
+def test_o_arena_from_tokens_places_each_items_rows(make):
+    # the dO layout the backward reads: every item's final block holds its rows and heads
+    import torch
+    w = make()
+    p = host_plan(w)
+    H, d, T = w.n_heads, w.head_dim, w.total_tokens
+    x = torch.arange(T * H * d, dtype=torch.float64).reshape(T, H, d)
+    arena = zl.o_arena_from_tokens(p, w.items, x)
+    assert arena.numel() == max(p.o_elems, 8)
+    for i, it in enumerate(w.items):
+        pl = p.item(i)
+        blk = arena[pl.fin_out_offset: pl.fin_out_offset + it.nq * it.nh * d].reshape(it.nq, it.nh, d)
+        s = it.seq_offset
+        assert torch.equal(blk, x[s + it.q_lo: s + it.q_hi, it.h_lo:it.h_hi])
+    # whole sequences sit in place, packed like the tokens
+    it = w.items[0]
+    if not it.emit_lse and it.nq == it.seq_len and it.nh == H:
+        s = it.seq_offset
+        assert torch.equal(arena[s * H * d:(s + it.seq_len) * H * d], x[s:s + it.seq_len].reshape(-1))

@@ -32,7 +32,7 @@ def _worker(rank, ws, port, out):
 def test_replicas_take_max_over_ranks():
     ws = 2
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork of a threaded process
     mp.spawn(_worker, args=(ws, port, out), nprocs=ws, join=True)
     for r in range(ws):
         v, t = out[r]
