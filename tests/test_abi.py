@@ -319,3 +319,44 @@ def test_o_arena_from_tokens_places_each_items_rows(make):
     if not it.emit_lse and it.nq == it.seq_len and it.nh == H:
         s = it.seq_offset
         assert torch.equal(arena[s * H * d:(s + it.seq_len) * H * d], x[s:s + it.seq_len].reshape(-1))
+
+
+def test_launches_reject_missing_and_host_only_plans(lib):
+    # every launch entry point returns ZL_ERR_INVALID_ARG for a null or host-only plan
+    # before it touches any pointer or the GPU (the dummy pointers are never read)
+    import ctypes
+    hp = host_plan(config_tiny())
+    x = ctypes.c_void_p(1 << 20)
+    f = ctypes.c_float(0.125)
+    calls = {
+        "zl_coalesced_attn_fwd": lambda p: lib.zl_coalesced_attn_fwd(p, x, x, x, x, x, x, f, None),
+        "zl_merge_partials": lambda p: lib.zl_merge_partials(p, x, x, x, x, None),
+        "zl_coalesced_attn_bwd": lambda p: lib.zl_coalesced_attn_bwd(p, x, x, x, x, x, x, x, x, x, x, f, None),
+        "zl_bwd_preprocess": lambda p: lib.zl_bwd_preprocess(p, x, x, x, None),
+        "zl_bwd_main": lambda p: lib.zl_bwd_main(p, x, x, x, x, x, x, x, x, f, None),
+        "zl_bwd_finalize": lambda p: lib.zl_bwd_finalize(p, x, x, f, None),
+        "zl_get_device_status": lambda p: lib.zl_get_device_status(p, None, ctypes.byref(ctypes.c_int32())),
+    }
+    for name, call in calls.items():
+        assert call(None) == zl.ZL_ERR_INVALID_ARG, name
+        assert call(hp.handle) == zl.ZL_ERR_INVALID_ARG, name
+
+
+def test_plan_queries_check_their_arguments(lib):
+    import ctypes
+    w = config_mixed()
+    p = host_plan(w)
+    I64, I32 = ctypes.c_int64, ctypes.c_int32
+    c = I64()
+    assert lib.zl_plan_count(p.handle, 5, ctypes.byref(c)) == zl.ZL_ERR_INVALID_ARG
+    assert lib.zl_plan_count(None, 0, ctypes.byref(c)) == zl.ZL_ERR_INVALID_ARG
+    assert lib.zl_plan_item(p.handle, len(w.items), None, None, None, None, None, None) == zl.ZL_ERR_INVALID_ARG
+    assert lib.zl_plan_item(p.handle, -1, None, None, None, None, None, None) == zl.ZL_ERR_INVALID_ARG
+    buf = (I32 * (4 * p.n_fwd_tiles))()
+    assert lib.zl_plan_tiles(p.handle, 2, buf, p.n_fwd_tiles) == zl.ZL_ERR_INVALID_ARG
+    assert lib.zl_plan_tiles(p.handle, 0, buf, p.n_fwd_tiles - 1) == zl.ZL_ERR_INVALID_ARG  # buffer too small
+    assert lib.zl_plan_tiles(p.handle, 0, buf, p.n_fwd_tiles) == zl.ZL_OK
+    assert lib.zl_plan_group(p.handle, p.n_groups, None, 0, None, None, None) == zl.ZL_ERR_INVALID_ARG
+    assert lib.zl_plan_arena_sizes(None, None, None, None, None, None, None) == zl.ZL_ERR_INVALID_ARG
+    assert lib.zl_plan_check_bounds(None) == zl.ZL_ERR_INVALID_ARG
+    assert lib.zl_plan_worklist(None, 0, 1, 64, 1, 0, None) == zl.ZL_ERR_INVALID_ARG
