@@ -28,6 +28,7 @@ def test_tiny_structured_peaky_softmax():
 @pytest.mark.parametrize("factor", [6])
 def test_images_scaled(factor):
     Run(scaled(config_images(), factor), seed=0).check_forward()
+    Run(scaled(config_images(), factor), seed=1, structured=True).check_forward()
 
 
 @pytest.mark.parametrize("factor", [12])
@@ -40,6 +41,7 @@ def test_mixed_shards_scaled(factor):
 @pytest.mark.parametrize("factor", [24])
 def test_long_video_k8_scaled(factor):
     Run(scaled(config_long_video(), factor), seed=0).check_forward()
+    Run(scaled(config_long_video(), factor), seed=1, structured=True).check_forward()
 
 
 @pytest.mark.parametrize("d", [64, 128])
