@@ -51,6 +51,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "zl_exp2.cuh"
 #include "zl_internal.h"
 #include "zl_kernels.h"
 #include "zl_ptx.cuh"
@@ -76,6 +77,23 @@ struct BwdLayout {
 };
 
 constexpr float kLog2eB = 1.44269504088896340736f;
+// Query pairs (bit e: queries 2e, 2e+1 of each 32-query half of a warpgroup's columns)
+// whose P exponents are computed on the FMA pipe (exp2_poly2) rather than the
+// special-function unit: every other pair (measured on the training list: 1.4 % faster
+// than all on the special-function unit; in the forward the same split was slower).
+#ifndef ZL_BWD_POLY_PAIRS
+#define ZL_BWD_POLY_PAIRS 0x5555u
+#endif
+constexpr uint32_t kPolyPairs = ZL_BWD_POLY_PAIRS;
+// dQ drain pacing: a warp's reductions of one block are spread over the previous block
+// period times 8 / ZL_DRAIN_SPREAD_EIGHTHS, or issued ZL_DRAIN_PACE_FIXED cycles apart
+// when that is set (> 0).
+#ifndef ZL_DRAIN_SPREAD_EIGHTHS
+#define ZL_DRAIN_SPREAD_EIGHTHS 9
+#endif
+#ifndef ZL_DRAIN_PACE_FIXED
+#define ZL_DRAIN_PACE_FIXED 0
+#endif
 constexpr float kInfB = __builtin_huge_valf();
 
 __device__ __forceinline__ void rec_err(int32_t* status, volatile int* abort_flag, int code) {
@@ -312,13 +330,18 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
     }
    } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (control flow, waits and descriptors are
+    // warp-uniform); one elected lane executes each product and commit.
+    {
       constexpr uint32_t kIdSq = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);
       constexpr uint32_t kIdDQ = idesc_bf16(128, D, true, true);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
                      aDS = smem_u32(sDS);
       const uint32_t tR0 = tmem, tR1 = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      auto wait_w = [&](uint64_t* b, uint32_t parity) {
+        return __all_sync(0xffffffffu, bwait(b, parity, abort_flag, p.wait_limit, p.status));
+      };
       // operand descriptors built once (K-major: LBO 16 B; MN-major: LBO one 16 KB box);
       // a K step or a ring slot only advances the start address
       // (low words only: all share the high word, see sdesc_join)
@@ -331,16 +354,17 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
       bool ok = true;
       while (ok) {
         const uint32_t slot = tile_it & 1;
-        if (!bwait(tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.wait_limit, p.status)) break;
+        if (!wait_w(tile_full + slot, (tile_it >> 1) & 1)) break;
         const int tid = ring[slot];
-        mbar_arrive(tile_empty + slot);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tile_empty + slot);
         ++tile_it;
         if (tid < 0) break;
         const DevTile tl = p.tiles[tid];
         const DevItem& it = p.items[tl.item];
         const int nqb = (it.q_hi - it.q_lo + kBlockM - 1) / kBlockM;
         if (nqb == 0) continue;
-        if (!bwait(kv_full, kt & 1, abort_flag, p.wait_limit, p.status)) break;
+        if (!wait_w(kv_full, kt & 1)) break;
         ++kt;
         tc_fence_after();
         // S^T = K Q^T of the query block in slot st (TMEM R0)
@@ -349,65 +373,64 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-            mma_ss(tR0, dsc(kK, off), dsc(dq, off), kIdSq, kk > 0);
+            mma_ss_w(tR0, dsc(kK, off), dsc(dq, off), kIdSq, kk > 0);
           }
-          mma_commit(s_full);
+          mma_commit_w(s_full);
         };
-        if (!bwait(q_full + (qit & 1), (qit >> 1) & 1, abort_flag, p.wait_limit, p.status)) break;
+        if (!wait_w(q_full + (qit & 1), (qit >> 1) & 1)) break;
         tc_fence_after();
         issue_s(qit & 1);
         for (int is = 0; is < nqb; ++is) {
           const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
-          if (!bwait(do_full + st, ph, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
-          if (nblocks > 0 && !bwait(dq_empty, (nblocks - 1) & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+          if (!wait_w(do_full + st, ph)) { ok = false; break; }
+          if (nblocks > 0 && !wait_w(dq_empty, (nblocks - 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-            mma_ss(tR1, dsc(kV, off), dsc(kDO, st * L::kTile + off), kIdSq, kk > 0);
+            mma_ss_w(tR1, dsc(kV, off), dsc(kDO, st * L::kTile + off), kIdSq, kk > 0);
           }
-          mma_commit(dp_full);
+          mma_commit_w(dp_full);
           // dV += P^T dO as soon as P^T is in TMEM (the warpgroup then forms dS^T)
-          if (!bwait(p_ready, nblocks & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+          if (!wait_w(p_ready, nblocks & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // K = 128 queries
-            mma_ts(tdV, tR0 + pcol(kk), dsc(mDO, st * L::kTile + kk * 2048), kIdKV,
-                   (is > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_w(tdV, tR0 + pcol(kk), dsc(mDO, st * L::kTile + kk * 2048), kIdKV,
+                     (is > 0 || kk > 0) ? 1u : 0u);
           if (is + 1 < nqb) {
             // S^T of the next block as soon as dV has read P^T out of R0 (one thread's
             // products run in issue order): the softmax warpgroups start on it while
             // this block's dK and dQ run
             const uint32_t st2 = (qit + 1) & 1, ph2 = ((qit + 1) >> 1) & 1;
-            if (!bwait(q_full + st2, ph2, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+            if (!wait_w(q_full + st2, ph2)) { ok = false; break; }
             tc_fence_after();
             issue_s(st2);
           }
-          if (!bwait(ds_ready, nblocks & 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+          if (!wait_w(ds_ready, nblocks & 1)) { ok = false; break; }
           tc_fence_after();
           // dQ first (R1 is free once the warpgroups have read dP^T): the drain warps start
           // on it while dK runs
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ = dS K   (K = 128 KV rows; both operands MN-major)
-            mma_ss(tR1, dsc(mDS, kk * 2048), dsc(mK, kk * 2048),
-                   kIdDQ, kk > 0);
-          mma_commit(dq_full);
+            mma_ss_w(tR1, dsc(mDS, kk * 2048), dsc(mK, kk * 2048), kIdDQ, kk > 0);
+          mma_commit_w(dq_full);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // dK += dS^T Q   (dS^T read K-major from shared memory)
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-            mma_ss(tdK, dsc(kDS, off), dsc(mQ, st * L::kTile + kk * 2048), kIdKV,
-                   (is > 0 || kk > 0) ? 1u : 0u);
+            mma_ss_w(tdK, dsc(kDS, off), dsc(mQ, st * L::kTile + kk * 2048), kIdKV,
+                     (is > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(q_empty + st);
+          mma_commit_w(q_empty + st);
           ++qit;
           ++nblocks;
         }
         if (!ok) break;
-        mma_commit(kv_done);
-        mma_commit(kv_empty);
+        mma_commit_w(kv_done);
+        mma_commit_w(kv_empty);
       }
-      mma_commit(drain);
-      bwait(drain, 0, abort_flag, p.wait_limit, p.status);
+      mma_commit_w(drain);
+      wait_w(drain, 0);
     }
    }
   } else if (warp >= 8) {
@@ -424,7 +447,7 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
     // faster than pacing at the lower bound, 1.4x faster than pacing by the period,
     // which includes the turn waits and so slows the successors in turn).
     constexpr long long kPaceMin = 48, kPaceMax = 160;
-    constexpr int kSpread = kReds + kReds / 8;
+    constexpr int kSpread = kReds * ZL_DRAIN_SPREAD_EIGHTHS / 8;
     const int t = threadIdx.x & 127;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t tile_it = 0, nblocks = 0;
@@ -464,6 +487,7 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         const long long t_full = clock64();
         long long pace = t_prev > 0 ? (t_full - t_prev) / kSpread : kPaceMin;
         pace = pace < kPaceMin ? kPaceMin : (pace > kPaceMax ? kPaceMax : pace);
+        if constexpr (ZL_DRAIN_PACE_FIXED > 0) pace = ZL_DRAIN_PACE_FIXED;
         if constexpr (kOrdered) pace = 0;
         t_prev = t_full;
         float* dst = acc + (int64_t)ib * (kBlockM * D);
@@ -573,15 +597,25 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           // exponent arguments two queries per instruction (the staged LSE is negated)
           const float2 sl2v = make_float2(sl2, sl2);
           const float2* nl2 = reinterpret_cast<const float2*>(sLSE + qc0);
+          // the pairs of kPolyPairs on the FMA pipe (exp2_poly2), the rest on the
+          // special-function unit; rows past the KV chunk get an exact 0
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float2 x0 = fma2(make_float2(__uint_as_float(u0[2 * e]), __uint_as_float(u0[2 * e + 1])), sl2v, nl2[e]);
             const float2 x1 =
                 fma2(make_float2(__uint_as_float(u1[2 * e]), __uint_as_float(u1[2 * e + 1])), sl2v, nl2[16 + e]);
-            pr[2 * e] = kv_ok ? ex2(x0.x) : 0.f;
-            pr[2 * e + 1] = kv_ok ? ex2(x0.y) : 0.f;
-            pr[32 + 2 * e] = kv_ok ? ex2(x1.x) : 0.f;
-            pr[32 + 2 * e + 1] = kv_ok ? ex2(x1.y) : 0.f;
+            float2 p0, p1;
+            if ((kPolyPairs >> e) & 1u) {
+              p0 = exp2_poly2<3>(x0);
+              p1 = exp2_poly2<3>(x1);
+            } else {
+              p0 = make_float2(ex2(x0.x), ex2(x0.y));
+              p1 = make_float2(ex2(x1.x), ex2(x1.y));
+            }
+            pr[2 * e] = kv_ok ? p0.x : 0.f;
+            pr[2 * e + 1] = kv_ok ? p0.y : 0.f;
+            pr[32 + 2 * e] = kv_ok ? p1.x : 0.f;
+            pr[32 + 2 * e + 1] = kv_ok ? p1.y : 0.f;
           }
         }
         // P^T (bf16) over this warpgroup's S^T columns, already read: dV may start now

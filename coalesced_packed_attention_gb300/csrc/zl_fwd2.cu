@@ -182,7 +182,9 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (control flow, waits and descriptors are
+    // warp-uniform); one elected lane executes each product and commit.
+    {
       constexpr uint32_t kIdS = idesc_bf16(128, kBlockN, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, D, false, true);
       const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
@@ -190,6 +192,9 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t qcount[2] = {0, 0};  // Q sub-tile loads consumed
       uint32_t pcount[2] = {0, 0};  // P handoffs consumed per sub-tile
       bool ok = true;
+      auto wait_w = [&](uint64_t* b, uint32_t parity) {
+        return __all_sync(0xffffffffu, wait2(b, parity, abort_flag, lim, p.status));
+      };
       // operand descriptors built once; a K step only advances the start address
       const uint64_t dQ0 = sdesc_sw128(aQ, 16, 1024), dK0 = sdesc_sw128(aK, 16, 1024);
       const uint64_t dV0 = sdesc_sw128(aV, L::kBox, 1024);
@@ -198,26 +203,27 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * L::kBox + (kk & 3) * 32;
-          mma_ss(tmem + 128 * w, sdesc_add(dq, koff), sdesc_add(dk, koff), kIdS, kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + 128 * w, sdesc_add(dq, koff), sdesc_add(dk, koff), kIdS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full + w);
+        mma_commit_w(s_full + w);
       };
       auto issue_pv = [&](int w, uint32_t stage, bool first) -> bool {
-        if (!wait2(p_full + w, pcount[w] & 1, abort_flag, lim, p.status)) return false;
+        if (!wait_w(p_full + w, pcount[w] & 1)) return false;
         ++pcount[w];
         tc_fence_after();
         const uint64_t dv = sdesc_add(dV0, stage * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem + 256 + 128 * w, tmem + 128 * w + kk * 8, sdesc_add(dv, kk * 2048), kIdPV,
-                 (first && kk == 0) ? 0u : 1u);
+          mma_ts_w(tmem + 256 + 128 * w, tmem + 128 * w + kk * 8, sdesc_add(dv, kk * 2048), kIdPV,
+                   (first && kk == 0) ? 0u : 1u);
         return true;
       };
       while (ok) {
         const uint32_t slot = tile_it & 1;
-        if (!wait2(tile_full + slot, (tile_it >> 1) & 1, abort_flag, lim, p.status)) break;
+        if (!wait_w(tile_full + slot, (tile_it >> 1) & 1)) break;
         const int tid = ring[slot];
-        mbar_arrive(tile_empty + slot);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tile_empty + slot);
         ++tile_it;
         if (tid < 0) break;
         const DevTile tl = p.tiles[tid];
@@ -228,37 +234,37 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t pstage = 0, pph = 0;
         for (int j = 0; j < nblk && ok; ++j) {
           const uint32_t s = kv_it % S, ph = (kv_it / S) & 1;
-          if (!wait2(k_full + s, ph, abort_flag, lim, p.status)) { ok = false; break; }
-          if (j > 0 && !wait2(v_full + pstage, pph, abort_flag, lim, p.status)) { ok = false; break; }
-          if (j == 0 && !wait2(q_full + 0, (qcount[0]++) & 1, abort_flag, lim, p.status)) { ok = false; break; }
+          if (!wait_w(k_full + s, ph)) { ok = false; break; }
+          if (j > 0 && !wait_w(v_full + pstage, pph)) { ok = false; break; }
+          if (j == 0 && !wait_w(q_full + 0, (qcount[0]++) & 1)) { ok = false; break; }
           tc_fence_after();
           if (j > 0 && !issue_pv(0, pstage, j == 1)) { ok = false; break; }
           issue_s(0, s);
           if (nsub == 2) {
-            if (j == 0 && !wait2(q_full + 1, (qcount[1]++) & 1, abort_flag, lim, p.status)) { ok = false; break; }
+            if (j == 0 && !wait_w(q_full + 1, (qcount[1]++) & 1)) { ok = false; break; }
             tc_fence_after();
             if (j > 0 && !issue_pv(1, pstage, j == 1)) { ok = false; break; }
             issue_s(1, s);
           }
-          if (j > 0) mma_commit(v_empty + pstage);
-          mma_commit(k_empty + s);
-          if (j == nblk - 1) mma_commit(q_empty);
+          if (j > 0) mma_commit_w(v_empty + pstage);
+          mma_commit_w(k_empty + s);
+          if (j == nblk - 1) mma_commit_w(q_empty);
           pstage = s; pph = ph;
           ++kv_it;
         }
         if (!ok) break;
-        if (!wait2(v_full + pstage, pph, abort_flag, lim, p.status)) break;
+        if (!wait_w(v_full + pstage, pph)) break;
         tc_fence_after();
         if (!issue_pv(0, pstage, nblk == 1)) break;
-        mma_commit(o_bar + 0);
+        mma_commit_w(o_bar + 0);
         if (nsub == 2) {
           if (!issue_pv(1, pstage, nblk == 1)) break;
-          mma_commit(o_bar + 1);
+          mma_commit_w(o_bar + 1);
         }
-        mma_commit(v_empty + pstage);
+        mma_commit_w(v_empty + pstage);
       }
-      mma_commit(drain);
-      wait2(drain, 0, abort_flag, lim, p.status);
+      mma_commit_w(drain);
+      wait_w(drain, 0);
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
