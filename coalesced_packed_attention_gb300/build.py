@@ -19,7 +19,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libzl.so")
-SOURCES = ["zl_plan.cpp", "zl_placement.cpp", "zl_api.cu", "zl_fwd.cu", "zl_fwd2.cu", "zl_bwd.cu", "zl_rowops.cu",
+SOURCES = ["zl_plan.cpp", "zl_placement.cpp", "zl_api.cu", "zl_fwd2.cu", "zl_bwd.cu", "zl_rowops.cu",
            "zl_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -86,9 +86,7 @@ extern "C" zl_status zl_coalesced_attn_fwd(const zl_plan* p, const void* q, cons
   fp.o_partial = o_partial;
   fp.lse = lse;
   fp.scale_log2 = scale * 1.44269504088896340736f;
-  cudaError_t e = p->fwd_block == kFwdBlockM
-                      ? launch_fwd2(p->head_dim, tq, tk, tv, fp, p->num_sms, static_cast<cudaStream_t>(stream))
-                      : launch_fwd(p->head_dim, tq, tk, tv, fp, p->num_sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fwd2(p->head_dim, tq, tk, tv, fp, p->num_sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
 
@@ -99,9 +97,12 @@ extern "C" zl_status zl_merge_partials(const zl_plan* p, const float* o_partial,
   if (p->merge_groups.empty()) return ZL_OK;  // none, or all fused into the forward
   if (!o_partial || !lse_partial || !o || !lse_out) return ZL_ERR_INVALID_ARG;
   if (!aligned16(o_partial) || !aligned16(lse_partial) || !aligned16(o) || !aligned16(lse_out)) return ZL_ERR_ALIGN;
+  int32_t max_members = 0;
+  for (const DevGroup& G : p->merge_groups) max_members = G.n_members > max_members ? G.n_members : max_members;
   cudaError_t e = launch_merge(p->head_dim, p->d_groups, (int32_t)p->merge_groups.size(), p->d_members,
-                               p->merge_rowheads, o_partial, lse_partial, static_cast<__nv_bfloat16*>(o), lse_out,
-                               p->num_sms, static_cast<cudaStream_t>(stream));
+                               p->merge_rowheads, max_members, o_partial, lse_partial,
+                               static_cast<__nv_bfloat16*>(o), lse_out, p->num_sms,
+                               static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
 
@@ -175,8 +176,8 @@ extern "C" zl_status zl_bwd_finalize(const zl_plan* p, float* dq, void* workspac
   if (!aligned16(dq) || !aligned16(workspace)) return ZL_ERR_ALIGN;
   if (p->items.empty()) return ZL_OK;
   const float* ws_dq = static_cast<const float*>(workspace) + p->ws_d_floats;
-  cudaError_t e = launch_dq_finalize(p->head_dim, p->d_items, p->n_user, p->total_rowheads, ws_dq,
-                                     dq, scale, p->num_sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_dq_finalize(p->head_dim, p->d_items, p->n_user, p->ws_dq_floats, ws_dq, dq, scale,
+                                     p->num_sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ZL_OK : ZL_ERR_CUDA;
 }
 

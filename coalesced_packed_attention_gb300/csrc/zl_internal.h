@@ -106,7 +106,6 @@ struct zl_plan {
   int num_sms = 0;
   bool host_only = false;
   bool test_withhold = false;   // ZL_PLAN_TEST_WITHHOLD_LOAD
-  int32_t fwd_block = zl::kFwdBlockM;  // query rows per forward tile: 256 (two sub-tiles) or 128
 
   std::vector<zl::DevItem> items;
   std::vector<zl_work_item> resolved;

@@ -41,15 +41,14 @@ struct BwdParams {
   float scale_log2;
 };
 
-cudaError_t launch_fwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int num_sms, cudaStream_t stream);
-
 cudaError_t launch_fwd2(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const FwdParams& p, int num_sms, cudaStream_t stream);
 
+// max_members: the largest member count of the groups (selects the kernel instance)
 cudaError_t launch_merge(int head_dim, const DevGroup* groups, int32_t n_groups, const DevMember* members,
-                         int64_t total_rowheads, const float* o_partial, const float* lse_partial,
-                         __nv_bfloat16* o, float* lse_out, int num_sms, cudaStream_t stream);
+                         int64_t total_rowheads, int32_t max_members, const float* o_partial,
+                         const float* lse_partial, __nv_bfloat16* o, float* lse_out, int num_sms,
+                         cudaStream_t stream);
 
 cudaError_t launch_bwd_pre(int head_dim, const DevItem* items, int32_t n_items, int64_t total_rowheads,
                            const __nv_bfloat16* o, const __nv_bfloat16* d_o, float* ws_d, float* ws_dq,
@@ -58,7 +57,8 @@ cudaError_t launch_bwd_pre(int head_dim, const DevItem* items, int32_t n_items, 
 cudaError_t launch_bwd(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const BwdParams& p, int num_sms, cudaStream_t stream);
 
-cudaError_t launch_dq_finalize(int head_dim, const DevItem* items, int32_t n_items, int64_t total_rowheads,
+// acc_floats_total: floats of the whole dQ accumulator (every item's, in item order)
+cudaError_t launch_dq_finalize(int head_dim, const DevItem* items, int32_t n_items, int64_t acc_floats_total,
                                const float* ws_dq, float* dq, float scale, int num_sms, cudaStream_t stream);
 
 }  // namespace zl

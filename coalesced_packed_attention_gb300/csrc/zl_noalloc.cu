@@ -25,6 +25,8 @@ namespace {
 // Every GPU that loads the library holds this array until the process exits.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
 constexpr size_t kCounterBytes = 256;                     // counter + status word, zeroed per call
+// The capacity stated in zl.h (bytes per item and per forward tile) follows these sizes.
+static_assert(sizeof(DevItem) == 112 && sizeof(DevTile) == 16, "update the capacity stated in zl.h");
 
 static __device__ __align__(256) unsigned char g_zl_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -146,4 +148,20 @@ extern "C" zl_status zl_coalesced_attn_fwd_noalloc(const zl_work_item* items, in
   }
   zl_plan_destroy(plan);  // host-only plan: frees host memory, no device call
   return s;
+}
+
+extern "C" zl_status zl_noalloc_get_device_status(void* stream, int32_t* device_status) {
+  if (!device_status) return ZL_ERR_INVALID_ARG;
+  ScratchSlot* slot = nullptr;
+  zl_status s = scratch_for_current_device(&slot);
+  if (s != ZL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* word = reinterpret_cast<int32_t*>(slot->base) + kStatus;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, word, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemsetAsync(word, 0, sizeof(int32_t), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return ZL_ERR_CUDA;
+  *device_status = v;
+  return ZL_OK;
 }

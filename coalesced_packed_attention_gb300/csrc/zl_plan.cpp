@@ -38,7 +38,15 @@ bool covers_sequence(const zl_work_item& it, int32_t H) {
   return it.q_lo == 0 && it.q_hi == it.seq_len && it.h_lo == 0 && it.h_hi == H;
 }
 
-zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
+using GroupKey = std::tuple<int64_t, int32_t, int32_t, int32_t, int32_t, int32_t>;
+GroupKey group_key(const zl_work_item& it) {
+  return std::make_tuple(it.seq_offset, it.seq_len, it.q_lo, it.q_hi, it.h_lo, it.h_hi);
+}
+
+// explicit: caller-chosen merge groups (member item ids in member order), or null for
+// the default grouping by equal (sequence, rows, heads) keys in list order.
+zl_status build(zl_plan* p, const zl_work_item* items, int32_t n,
+                const std::vector<std::vector<int32_t>>* explicit_groups) {
   const int32_t H = p->n_heads, d = p->head_dim;
   const int64_t T = p->total_tokens;
   for (int32_t i = 0; i < n; ++i) {
@@ -46,25 +54,42 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
     if (s != ZL_OK) return s;
   }
 
-  // ---- merge groups: emit_lse items sharing (sequence, rows, heads), list order
-  std::map<std::tuple<int64_t, int32_t, int32_t, int32_t, int32_t, int32_t>, int32_t> gkey;
+  // ---- merge groups
   std::vector<std::vector<int32_t>> gmembers;
   p->item_group.assign(n, -1);
-  for (int32_t i = 0; i < n; ++i) {
-    const zl_work_item& it = items[i];
-    if (!it.emit_lse) continue;
-    auto key = std::make_tuple(it.seq_offset, it.seq_len, it.q_lo, it.q_hi, it.h_lo, it.h_hi);
-    auto f = gkey.find(key);
-    int32_t g;
-    if (f == gkey.end()) {
-      g = (int32_t)gmembers.size();
-      gkey[key] = g;
-      gmembers.emplace_back();
-    } else {
-      g = f->second;
+  if (explicit_groups) {
+    // every emit_lse item in exactly one group, every member an emit_lse item, members
+    // of a group sharing sequence, rows and heads
+    for (size_t g = 0; g < explicit_groups->size(); ++g) {
+      const std::vector<int32_t>& m = (*explicit_groups)[g];
+      if (m.empty()) return ZL_ERR_INVALID_ARG;
+      for (int32_t i : m) {
+        if (i < 0 || i >= n || !items[i].emit_lse || p->item_group[i] >= 0) return ZL_ERR_INVALID_ARG;
+        if (group_key(items[i]) != group_key(items[m[0]])) return ZL_ERR_INVALID_ARG;
+        p->item_group[i] = (int32_t)g;
+      }
     }
-    gmembers[g].push_back(i);
-    p->item_group[i] = g;
+    for (int32_t i = 0; i < n; ++i)
+      if (items[i].emit_lse && p->item_group[i] < 0) return ZL_ERR_INVALID_ARG;
+    gmembers = *explicit_groups;
+  } else {
+    // emit_lse items sharing (sequence, rows, heads), list order
+    std::map<GroupKey, int32_t> gkey;
+    for (int32_t i = 0; i < n; ++i) {
+      const zl_work_item& it = items[i];
+      if (!it.emit_lse) continue;
+      auto f = gkey.find(group_key(it));
+      int32_t g;
+      if (f == gkey.end()) {
+        g = (int32_t)gmembers.size();
+        gkey[group_key(it)] = g;
+        gmembers.emplace_back();
+      } else {
+        g = f->second;
+      }
+      gmembers[g].push_back(i);
+      p->item_group[i] = g;
+    }
   }
   // KV chunks of one group must be disjoint; with ZL_PLAN_FUSE_LOCAL_KMERGE a group
   // whose chunks tile one contiguous range [kv_lo, kv_hi) is computed as one item
@@ -227,7 +252,7 @@ zl_status build(zl_plan* p, const zl_work_item* items, int32_t n) {
     const DevItem& it = p->items[i];
     const bool user = i < n;
     const int32_t nqb = (int32_t)ceil_div(it.q_hi - it.q_lo, kBlockM);
-    const int32_t nfb = (int32_t)ceil_div(it.q_hi - it.q_lo, p->fwd_block);
+    const int32_t nfb = (int32_t)ceil_div(it.q_hi - it.q_lo, kFwdBlockM);
     const int32_t nkb = (int32_t)ceil_div(it.kv_hi - it.kv_lo, kBlockN);
     const bool fwd = !user || !fused_member(i);
     for (int32_t h = it.h_lo; h < it.h_hi; ++h) {
@@ -295,16 +320,20 @@ zl_status upload(zl_plan* p) {
 
 }  // namespace
 
-extern "C" zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items, int32_t n_heads,
-                                      int32_t head_dim, int64_t total_tokens, uint32_t flags,
-                                      zl_plan** out) {
-  NvtxRange range("zl_plan_worklist");
+namespace {
+
+zl_status plan_impl(const zl_work_item* items, int32_t n_items, int32_t n_heads, int32_t head_dim,
+                    int64_t total_tokens, uint32_t flags, const std::vector<std::vector<int32_t>>* groups,
+                    zl_plan** out) {
   if (!out) return ZL_ERR_INVALID_ARG;
   *out = nullptr;
   if (n_items < 0 || (n_items > 0 && !items) || n_heads < 1 || total_tokens < 1 ||
       total_tokens >= ((int64_t)1 << 31))
     return ZL_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return ZL_ERR_UNSUPPORTED;
+  constexpr uint32_t kKnownFlags =
+      ZL_PLAN_HOST_ONLY | ZL_PLAN_TEST_WITHHOLD_LOAD | ZL_PLAN_FUSE_LOCAL_KMERGE | ZL_PLAN_DETERMINISTIC_DQ;
+  if (flags & ~kKnownFlags) return ZL_ERR_INVALID_ARG;
   zl_plan* p = new (std::nothrow) zl_plan();
   if (!p) return ZL_ERR_NO_MEMORY;
   p->n_heads = n_heads;
@@ -312,10 +341,9 @@ extern "C" zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items
   p->total_tokens = total_tokens;
   p->host_only = (flags & ZL_PLAN_HOST_ONLY) != 0;
   p->test_withhold = (flags & ZL_PLAN_TEST_WITHHOLD_LOAD) != 0;
-  p->fwd_block = (flags & ZL_PLAN_FWD_ONE_SUBTILE) ? kBlockM : kFwdBlockM;
   p->fuse_kmerge = (flags & ZL_PLAN_FUSE_LOCAL_KMERGE) != 0;
   p->det_dq = (flags & ZL_PLAN_DETERMINISTIC_DQ) != 0;
-  zl_status s = build(p, items, n_items);
+  zl_status s = build(p, items, n_items, groups);
   if (s == ZL_OK && p->det_dq) s = zl_plan_check_bounds(p);  // includes the turn order
   if (s == ZL_OK && !p->host_only) s = upload(p);
   if (s != ZL_OK) {
@@ -324,6 +352,31 @@ extern "C" zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items
   }
   *out = p;
   return ZL_OK;
+}
+
+}  // namespace
+
+extern "C" zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items, int32_t n_heads,
+                                      int32_t head_dim, int64_t total_tokens, uint32_t flags,
+                                      zl_plan** out) {
+  NvtxRange range("zl_plan_worklist");
+  return plan_impl(items, n_items, n_heads, head_dim, total_tokens, flags, nullptr, out);
+}
+
+extern "C" zl_status zl_plan_worklist_groups(const zl_work_item* items, int32_t n_items, int32_t n_heads,
+                                             int32_t head_dim, int64_t total_tokens, uint32_t flags,
+                                             const int32_t* group_item_ids, const int32_t* group_ptr,
+                                             int32_t n_groups, zl_plan** out) {
+  NvtxRange range("zl_plan_worklist_groups");
+  if (out) *out = nullptr;
+  if (n_groups < 0 || (n_groups > 0 && (!group_item_ids || !group_ptr)) || (group_ptr && group_ptr[0] != 0))
+    return ZL_ERR_INVALID_ARG;
+  std::vector<std::vector<int32_t>> groups((size_t)n_groups);
+  for (int32_t g = 0; g < n_groups; ++g) {
+    if (group_ptr[g + 1] < group_ptr[g] || group_ptr[g + 1] > (int64_t)n_items) return ZL_ERR_INVALID_ARG;
+    groups[g].assign(group_item_ids + group_ptr[g], group_item_ids + group_ptr[g + 1]);
+  }
+  return plan_impl(items, n_items, n_heads, head_dim, total_tokens, flags, &groups, out);
 }
 
 extern "C" void zl_plan_destroy(zl_plan* plan) {
@@ -445,7 +498,7 @@ extern "C" zl_status zl_plan_check_bounds(const zl_plan* p) {
   for (const auto& t : p->fwd_tiles) {
     if (t.item < 0 || t.item >= n) return ZL_ERR_INVALID_ARG;
     const DevItem& it = p->items[t.item];
-    if (t.head < it.h_lo || t.head >= it.h_hi || (int64_t)t.block * p->fwd_block >= it.q_hi - it.q_lo)
+    if (t.head < it.h_lo || t.head >= it.h_hi || (int64_t)t.block * kFwdBlockM >= it.q_hi - it.q_lo)
       return ZL_ERR_INVALID_ARG;
   }
   // deterministic dQ: the KV tiles of each (item, head) must be claimed in the order of

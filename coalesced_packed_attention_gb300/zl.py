@@ -18,7 +18,6 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libzl.so")
 ZL_OK, ZL_ERR_INVALID_ARG, ZL_ERR_ALIGN, ZL_ERR_CUDA, ZL_ERR_TIMEOUT, ZL_ERR_UNSUPPORTED, ZL_ERR_NO_MEMORY = range(7)
 ZL_PLAN_HOST_ONLY = 1
 ZL_PLAN_TEST_WITHHOLD_LOAD = 2
-ZL_PLAN_FWD_ONE_SUBTILE = 4
 ZL_PLAN_FUSE_LOCAL_KMERGE = 8
 ZL_PLAN_DETERMINISTIC_DQ = 16
 
@@ -60,6 +59,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     pD = ctypes.POINTER(ctypes.c_double)
     sig = {
         "zl_plan_worklist": (I32, [ctypes.POINTER(zl_work_item), I32, I32, I32, I64, U32, ctypes.POINTER(P)]),
+        "zl_plan_worklist_groups": (I32, [ctypes.POINTER(zl_work_item), I32, I32, I32, I64, U32, pI32, pI32, I32,
+                                          ctypes.POINTER(P)]),
         "zl_plan_destroy": (None, [P]),
         "zl_plan_arena_sizes": (I32, [P, pI64, pI64, pI64, pI64, pI64, pI64]),
         "zl_plan_item": (I32, [P, I32, ctypes.POINTER(zl_work_item), pI64, pI64, pI64, pI64, pI32]),
@@ -182,18 +183,39 @@ def _to_c_items(items: Sequence) -> ctypes.Array:
     return arr
 
 
+def _plan_device(flags: int):
+    if flags & ZL_PLAN_HOST_ONLY:
+        return None
+    import torch
+    return torch.cuda.current_device() if torch.cuda.is_available() else None  # else the library reports it
+
+
 def zl_plan_worklist(items: Sequence, n_heads: int, head_dim: int, total_tokens: int, flags: int = 0) -> Plan:
     L = load_library()
     h = ctypes.c_void_p()
-    host_only = bool(flags & ZL_PLAN_HOST_ONLY)
-    device = None
-    if not host_only:
-        import torch
-        if torch.cuda.is_available():  # else the library reports the missing device
-            device = torch.cuda.current_device()
+    device = _plan_device(flags)
     _check(L.zl_plan_worklist(_to_c_items(items), len(items), n_heads, head_dim, total_tokens, flags,
                               ctypes.byref(h)), "zl_plan_worklist")
-    return Plan(h.value, n_heads, head_dim, total_tokens, host_only, device)
+    return Plan(h.value, n_heads, head_dim, total_tokens, bool(flags & ZL_PLAN_HOST_ONLY), device)
+
+
+def zl_plan_worklist_groups(items: Sequence, n_heads: int, head_dim: int, total_tokens: int,
+                            groups: Sequence[Sequence[int]], flags: int = 0) -> Plan:
+    """zl_plan_worklist with caller-chosen merge groups: groups[g] lists the work-list
+    indices of group g's emit_lse items in member order (passed as group_item_ids /
+    group_ptr)."""
+    L = load_library()
+    h = ctypes.c_void_p()
+    ids = [int(i) for g in groups for i in g]
+    ptr = [0]
+    for g in groups:
+        ptr.append(ptr[-1] + len(g))
+    c_ids = (ctypes.c_int32 * max(1, len(ids)))(*ids)
+    c_ptr = (ctypes.c_int32 * len(ptr))(*ptr)
+    device = _plan_device(flags)
+    _check(L.zl_plan_worklist_groups(_to_c_items(items), len(items), n_heads, head_dim, total_tokens, flags, c_ids,
+                                     c_ptr, len(groups), ctypes.byref(h)), "zl_plan_worklist_groups")
+    return Plan(h.value, n_heads, head_dim, total_tokens, bool(flags & ZL_PLAN_HOST_ONLY), device)
 
 
 # ---------------------------------------------------------------- launches
@@ -356,7 +378,7 @@ def backward(plan: Plan, q, k, v, d_o, scale: float, bufs: dict, stream=None) ->
 
 def exported_symbols() -> List[str]:
     """Names of the entry points declared in include/zl.h."""
-    return ["zl_plan_worklist", "zl_plan_destroy", "zl_plan_arena_sizes", "zl_plan_item", "zl_plan_check_bounds",
+    return ["zl_plan_worklist", "zl_plan_worklist_groups", "zl_plan_destroy", "zl_plan_arena_sizes", "zl_plan_item", "zl_plan_check_bounds",
             "zl_plan_count",
             "zl_plan_tiles", "zl_plan_group", "zl_coalesced_attn_fwd", "zl_merge_partials",
             "zl_coalesced_attn_bwd", "zl_bwd_preprocess", "zl_bwd_main", "zl_bwd_finalize",

@@ -99,10 +99,7 @@ typedef struct zl_plan zl_plan;
  * wait runs out (after ~20M cycles) and zl_get_device_status reports ZL_ERR_TIMEOUT;
  * nothing faults or hangs. */
 #define ZL_PLAN_TEST_WITHHOLD_LOAD 2u
-/* Forward variant: tiles of 128 query rows with one softmax warpgroup per CTA instead
- * of the default 256-row tiles split into two 128-row sub-tiles whose softmax
- * warpgroups alternate on the tensor core.  Both compute the same result. */
-#define ZL_PLAN_FWD_ONE_SUBTILE 4u
+/* (Flag value 4 is not used; zl_plan_worklist rejects flags it does not know.) */
 /* Fused local k-merge.  A merge group (emit_lse items sharing sequence, rows and heads)
  * whose KV chunks tile one contiguous range is computed by the forward launch as a
  * single item over that range: its final O (bf16) and LSE go straight into the group's
@@ -132,9 +129,12 @@ typedef struct zl_plan zl_plan;
 
 /* Validate a work list and build its tile lists (host C++), then upload them to the
  * current device.
+ * Passage: pith.science review, "What carries the argument" (theta=(q,h,k) cuts a
+ * sequence into query-row, head and KV shards; the engine schedules whole sequences and
+ * shards that share a rank in a fixed order and fuses them into shared launches).
  *   items[n_items]: descriptors (host memory, read only; not retained).
  *   n_heads H >= 1, head_dim d in {64, 128}, total_tokens T >= 1 (Q/K/V have T rows).
- * Tiles: forward = (item, head, 256 query rows; 128 with ZL_PLAN_FWD_ONE_SUBTILE);
+ * Tiles: forward = (item, head, 256 query rows, run as two 128-row sub-tiles);
  * backward = (item, head, 128 KV rows).
  * Each list is sorted longest-first (cost = KV blocks for forward, query blocks for
  * backward), ties in work-list order, and a persistent grid of one CTA per SM claims
@@ -148,18 +148,37 @@ ZL_API zl_status zl_plan_worklist(const zl_work_item* items, int32_t n_items, in
                            int32_t head_dim, int64_t total_tokens, uint32_t flags,
                            zl_plan** out);
 
-/* Free a plan (host and device parts).  NULL is ignored.  Must not be called while a
+/* Passage: as zl_plan_worklist and zl_merge_partials.  zl_plan_worklist with the merge
+ * groups chosen by the caller instead of formed from equal (sequence, q range, h range)
+ * keys in list order.  Group g holds the emit_lse items
+ * group_item_ids[group_ptr[g] .. group_ptr[g+1]) (host arrays; group_ptr has n_groups + 1
+ * entries, group_ptr[0] = 0), merged in that member order.  Every emit_lse item must be
+ * in exactly one group; the members of a group must share sequence, q range and h range,
+ * and their KV chunks must be disjoint.  A group is one exact attention problem over the
+ * union of its members' chunks: its merged O and LSE are the final outputs its members'
+ * backward reads, so two groups over the same rows and heads are two separate problems
+ * (e.g. two KV subsets of one sequence).  The groups are fixed here rather than given to
+ * zl_merge_partials because the plan places each group's output block and the backward of
+ * every member reads it.  Errors: as zl_plan_worklist, and ZL_ERR_INVALID_ARG for a
+ * malformed group_ptr, an item id out of range, a member without emit_lse, an emit_lse
+ * item in no group or in two, or members with different keys. */
+ZL_API zl_status zl_plan_worklist_groups(const zl_work_item* items, int32_t n_items, int32_t n_heads,
+                                         int32_t head_dim, int64_t total_tokens, uint32_t flags,
+                                         const int32_t* group_item_ids, const int32_t* group_ptr,
+                                         int32_t n_groups, zl_plan** out);
+
+/* Free a plan (host and device parts).  (Library mechanics; no passage.)  NULL is ignored.  Must not be called while a
  * launch that uses the plan is still running. */
 ZL_API void zl_plan_destroy(zl_plan* plan);
 
 /* Element counts of every arena the caller must allocate for this plan (any pointer
- * may be NULL).  workspace_bytes: scratch for zl_coalesced_attn_bwd (row sums D, the
+ * may be NULL).  Passage: as zl_plan_worklist (every item and shard owns its blocks).  workspace_bytes: scratch for zl_coalesced_attn_bwd (row sums D, the
  * fp32 dQ accumulator and, with ZL_PLAN_DETERMINISTIC_DQ, its turn counters). */
 ZL_API zl_status zl_plan_arena_sizes(const zl_plan* plan, int64_t* o_elems, int64_t* o_partial_elems,
                               int64_t* lse_elems, int64_t* dq_elems, int64_t* dkv_elems,
                               int64_t* workspace_bytes);
 
-/* Resolved placement of item i: its descriptor with offsets filled in, plus
+/* Passage: as zl_plan_worklist.  Resolved placement of item i: its descriptor with offsets filled in, plus
  * fin_out_offset / fin_lse_offset (where its FINAL O, dO and LSE live in `o` / `lse`:
  * its own block, or its merge group's block for an emit_lse item), dq_offset and
  * dkv_offset (its gradient blocks), and group (merge group index or -1). */
@@ -167,27 +186,33 @@ ZL_API zl_status zl_plan_item(const zl_plan* plan, int32_t i, zl_work_item* reso
                        int64_t* fin_out_offset, int64_t* fin_lse_offset, int64_t* dq_offset,
                        int64_t* dkv_offset, int32_t* group);
 
-/* Host-side dry run of the plan: every block and workspace range that a launch with
+/* (Library mechanics, standing in for a device-side bounds checker; no passage.)
+ * Host-side dry run of the plan: every block and workspace range that a launch with
  * this plan would touch lies inside the arena sizes of zl_plan_arena_sizes, and every
  * tile addresses an existing item, head and block.  ZL_OK or ZL_ERR_INVALID_ARG.  Works
  * on host-only plans (no GPU needed). */
 ZL_API zl_status zl_plan_check_bounds(const zl_plan* plan);
 
-/* Counts: which = 0 forward tiles, 1 backward tiles, 2 merge groups, 3 items (of the
+/* Passage: as zl_plan_worklist.  Counts: which = 0 forward tiles, 1 backward tiles, 2 merge groups, 3 items (of the
  * work list), 4 merge groups that zl_merge_partials combines (2 minus those fused into
  * the forward by ZL_PLAN_FUSE_LOCAL_KMERGE). */
 ZL_API zl_status zl_plan_count(const zl_plan* plan, int32_t which, int64_t* count);
 
-/* Copy a tile list to host memory as n x 4 int32 {item, head, block, cost}, in the
+/* Passage: as zl_plan_worklist (the fixed order in which shared launches take the work).
+ * Copy a tile list to host memory as n x 4 int32 {item, head, block, cost}, in the
  * order the scheduler hands tiles out.  which = 0 forward, 1 backward. */
 ZL_API zl_status zl_plan_tiles(const zl_plan* plan, int32_t which, int32_t* out, int64_t n);
 
-/* Merge group g: member item ids (up to cap written), member count, and the group's
+/* Passage: as zl_merge_partials.  Merge group g: member item ids (up to cap written), member count, and the group's
  * final O / LSE offsets in `o` / `lse`. */
 ZL_API zl_status zl_plan_group(const zl_plan* plan, int32_t g, int32_t* members, int32_t cap,
                         int32_t* n_members, int64_t* out_offset, int64_t* lse_offset);
 
-/* Forward: one persistent launch over every forward tile of the plan (sm_103a:
+/* Passage: newx.sg page, Abstract (the coalesced attention engine runs whole sequences
+ * alongside distributed-attention shards); pith.science review, "What carries the
+ * argument" (whole sequences and shards fused on a shared rank) and "Assumptions & free
+ * parameters" (exact attention, FlashAttention [7]).
+ * Forward: one persistent launch over every forward tile of the plan (sm_103a:
  * TMA-staged Q/K/V tiles, tcgen05 MMA with TMEM accumulators for S = Q K^T and
  * O += P V, online softmax with base-2 exponent, LSE epilogue).
  *   q, k, v: bf16 [T, H, d] device pointers (read only).
@@ -195,14 +220,20 @@ ZL_API zl_status zl_plan_group(const zl_plan* plan, int32_t g, int32_t* members,
  *   o_partial: fp32 arena for emit_lse = 1 items; may be NULL if there are none.
  *   lse: fp32 arena; every item writes its LSE block (partial LSE for emit_lse items).
  *   scale: softmax scale applied to Q K^T (1/sqrt(d) for DiT attention).
- * Items with an empty KV range write O = 0 and LSE = -inf.  Inputs must be finite.
- * Tail rows past an item's q_hi are computed from neighbouring tokens but never
- * stored. */
+ * Items with an empty KV range write O = 0 and LSE = -inf.
+ * Every token of q, k and v must be finite, including tokens that belong to no item: the
+ * last, partial 128-row tile of an item reads the tokens that follow it in the packed
+ * tensors, and although their scores are masked and their rows are never stored, a
+ * value row past the item's KV range is still multiplied by a zero weight, so a NaN or
+ * Inf there would reach the item's output. */
 ZL_API zl_status zl_coalesced_attn_fwd(const zl_plan* plan, const void* q, const void* k,
                                 const void* v, void* o, float* o_partial, float* lse,
                                 float scale, void* stream);
 
-/* Merge every k-split group of the plan: with M = max_c LSE_c,
+/* Passage: pith.science review, "What carries the argument" (the k of theta splits the
+ * key/value states) and its ref. [19], ring attention, which combines per-chunk partial
+ * outputs by their log-sum-exp weights; the pages do not print the combine.
+ * Merge every k-split group of the plan: with M = max_c LSE_c,
  * LSE = M + ln sum_c exp(LSE_c - M) and O = sum_c exp(LSE_c - LSE) O_c.
  * Reads o_partial and the members' LSE blocks from lse_partial; writes the group's bf16
  * O block into o and its LSE block into lse_out (lse_out may equal lse_partial: the
@@ -211,7 +242,10 @@ ZL_API zl_status zl_coalesced_attn_fwd(const zl_plan* plan, const void* q, const
 ZL_API zl_status zl_merge_partials(const zl_plan* plan, const float* o_partial,
                             const float* lse_partial, void* o, float* lse_out, void* stream);
 
-/* Backward of every item, using each item's FINAL output and LSE (for k-split items,
+/* Passage: newx.sg page, Abstract (DiT training on image and video data: the engine runs
+ * the training step's attention, so its gradient too); pith.science review, "What carries
+ * the argument" (theta shards; a shard's gradients are its own block's contribution).
+ * Backward of every item, using each item's FINAL output and LSE (for k-split items,
  * the merged group's O and global LSE):
  *   D_i = rowsum(dO_i * O_i);  P_ij = exp(s_ij - LSE_i);  dS_ij = P_ij (dO_i.V_j - D_i);
  *   dV_j = sum_i P_ij dO_i;  dK_j = scale sum_i dS_ij Q_i;  dQ_i = scale sum_j dS_ij K_j,
@@ -221,13 +255,16 @@ ZL_API zl_status zl_merge_partials(const zl_plan* plan, const float* o_partial,
  *   dq, dk, dv: fp32 gradient arenas (written, not accumulated).
  *   workspace: device scratch of zl_plan_arena_sizes' workspace_bytes (16-byte aligned).
  * Launches: row sums D + zeroing of the dQ accumulator; the persistent tcgen05
- * backward over (item, head, 128 KV rows) tiles; the dQ finalisation (scale). */
+ * backward over (item, head, 128 KV rows) tiles; the dQ finalisation (scale).
+ * As for the forward, every token of q, k and v must be finite (partial tiles read the
+ * tokens that follow an item and multiply them by zero weights). */
 ZL_API zl_status zl_coalesced_attn_bwd(const zl_plan* plan, const void* q, const void* k,
                                 const void* v, const void* o, const void* d_o,
                                 const float* lse, float* dq, float* dk, float* dv,
                                 void* workspace, float scale, void* stream);
 
-/* The three launches of zl_coalesced_attn_bwd, callable one by one (same arguments,
+/* Passage: as zl_coalesced_attn_bwd.
+ * The three launches of zl_coalesced_attn_bwd, callable one by one (same arguments,
  * same order of use); zl_coalesced_attn_bwd is exactly these three in sequence.
  *   zl_bwd_preprocess: D_i = rowsum(dO_i * O_i) into the workspace and zeroing of the
  *     workspace's fp32 dQ accumulator (and turn counters) (HBM-bound, one warp per
@@ -254,28 +291,42 @@ ZL_API zl_status zl_bwd_finalize(const zl_plan* plan, float* dq, void* workspace
  *   a host-only plan, ZL_PLAN_HOST_ONLY, for the offsets and arena sizes).
  *   Scratch: the item table, tile list, scheduler counter and status word live in a
  *   fixed 8 MiB array compiled into the library; every GPU that loads the library holds
- *   it until the process exits.  A list whose tables do not fit (about 500 000 tiles of
- *   256 query rows) is rejected with ZL_ERR_INVALID_ARG before any device work.
- *   The first call on a device looks up that array's device address (once per device,
- *   with the device current); make that first call before any stream capture.
+ *   it until the process exits.  Capacity: 112 bytes per work item plus 16 bytes per
+ *   forward tile (256 query rows of one head), each table rounded up to 256 bytes,
+ *   within 8 MiB - 256 bytes: about 65 000 items of one tile each, or about 520 000
+ *   tiles over a few items.  A larger list is rejected with ZL_ERR_INVALID_ARG before
+ *   any device work.
+ *   The first call on a device (of this or of zl_noalloc_get_device_status) looks up that
+ *   array's device address (once per device, with the device current); make that first
+ *   call before any stream capture.
  *   Every call shares the array and zeroes the counter and status word itself, so calls
  *   whose launches overlap on the GPU (different streams, different threads) race on
- *   it: order them.  The device status word is not reported by this entry point.
+ *   it: order them.  A bounded device wait that gives up is recorded in the array's
+ *   status word: read it with zl_noalloc_get_device_status after the call and before the
+ *   next one (the next call clears it).
  *   Calls no cudaMalloc/cudaFree or other allocating routine. */
 ZL_API zl_status zl_coalesced_attn_fwd_noalloc(const zl_work_item* items, int32_t n_items, int32_t n_heads,
                                                int32_t head_dim, int64_t total_tokens, const void* q,
                                                const void* k, const void* v, void* o, float* o_partial,
                                                float* lse, float scale, void* stream);
 
-/* Read and clear the plan's device status word (synchronises `stream`).  *device_status
+/* Status word of zl_coalesced_attn_fwd_noalloc on the current device (no counterpart in
+ * the paper): synchronises `stream`, stores in *device_status ZL_OK or the first error
+ * the last call's kernel recorded (ZL_ERR_TIMEOUT when a bounded wait gave up; the kernel
+ * then stopped cleanly instead of hanging, and its outputs are incomplete), and clears
+ * the word.  Allocates nothing.  ZL_ERR_INVALID_ARG for a NULL device_status. */
+ZL_API zl_status zl_noalloc_get_device_status(void* stream, int32_t* device_status);
+
+/* (Library mechanics: failure detection by bounded device waits; no passage.)
+ * Read and clear the plan's device status word (synchronises `stream`).  *device_status
  * receives ZL_OK or the first error a kernel recorded (ZL_ERR_TIMEOUT when a bounded
  * wait gave up; the kernel then stopped cleanly instead of hanging). */
 ZL_API zl_status zl_get_device_status(const zl_plan* plan, void* stream, int32_t* device_status);
 
-/* Static text for a status code. */
+/* Static text for a status code.  (Library mechanics; no passage.) */
 ZL_API const char* zl_status_string(zl_status status);
 
-/* Library version, e.g. 100 for 0.1.0. */
+/* Library version, e.g. 100 for 0.1.0.  (Library mechanics; no passage.) */
 ZL_API int32_t zl_version(void);
 
 /* ------------------------------------------------------------------------------------
@@ -298,7 +349,9 @@ typedef struct {
   double mem;     /* >= 0 */
 } zl_bucket;
 
-/* Catalog cut.  buckets[n_buckets] sorted by time ascending (host memory, read only).
+/* Passage: pith.science review, "Assumptions & free parameters" (catalog cut k*, Eq. 4:
+ * the split that minimises the within-set dispersion of log whole-sequence times).
+ * Catalog cut.  buckets[n_buckets] sorted by time ascending (host memory, read only).
  * With x_b = ln time_b and the count-weighted means mu_F, mu_A of x over buckets
  * [0, k) and [k, n), the cut k in 1..n-1 minimises
  *   D(k) = sum_{b<k} count_b (x_b - mu_F)^2 + sum_{b>=k} count_b (x_b - mu_A)^2;
@@ -308,7 +361,9 @@ typedef struct {
  * finite, or buckets out of order. */
 ZL_API zl_status zl_catalog_cut(const zl_bucket* buckets, int32_t n_buckets, int32_t* k_star, double* dispersion);
 
-/* Filler packing.  Places fillers s = 0..n_fillers-1 (time filler_time[s], memory
+/* Passage: pith.science review, "What carries the argument" (whole filler sequences
+ * packed greedily by a bottleneck score) and its referee report on Eq. (8).
+ * Filler packing.  Places fillers s = 0..n_fillers-1 (time filler_time[s], memory
  * filler_mem[s]; host arrays) whole on n_ranks ranks that already carry rank_time[r],
  * rank_mem[r] (the anchors' load; NULL = zeros).  Fillers go in decreasing time (ties:
  * lower index first), each to the rank with the largest bottleneck score

@@ -1,5 +1,6 @@
 """The C-ABI library loads and exports every entry point include/zl.h declares; the
 host planner's validation, placement and tiling (host-only plans, no GPU)."""
+import ctypes
 import os
 import re
 
@@ -31,8 +32,8 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
     assert sorted(zl.exported_symbols()) == sorted(n for n in names if n in zl.exported_symbols())
     # every declared entry point has a Python binding, except the allocation-free
-    # forward, whose callers (and its test) use the C ABI directly
-    assert set(names) - {"zl_coalesced_attn_fwd_noalloc"} <= set(zl.exported_symbols())
+    # forward and its status query, whose callers (and its test) use the C ABI directly
+    assert set(names) - {"zl_coalesced_attn_fwd_noalloc", "zl_noalloc_get_device_status"} <= set(zl.exported_symbols())
 
 
 def test_status_strings(lib):
@@ -58,6 +59,13 @@ def host_plan(work):
 def test_invalid_items_are_rejected(bad):
     with pytest.raises(zl.ZlError) as e:
         zl.zl_plan_worklist([bad], 4, 64, 1000, flags=zl.ZL_PLAN_HOST_ONLY)
+    assert e.value.status == zl.ZL_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("flags", [4, 32, 1 << 31])
+def test_unknown_plan_flags_are_rejected(flags):
+    with pytest.raises(zl.ZlError) as e:
+        zl.zl_plan_worklist([WorkItem(0, 100, 0, 100, 0, 4, 0, 100)], 4, 64, 1000, flags=zl.ZL_PLAN_HOST_ONLY | flags)
     assert e.value.status == zl.ZL_ERR_INVALID_ARG
 
 
@@ -169,7 +177,7 @@ def _all_lists():
     return lists
 
 
-@pytest.mark.parametrize("flags", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE, zl.ZL_PLAN_FUSE_LOCAL_KMERGE,
+@pytest.mark.parametrize("flags", [0, zl.ZL_PLAN_FUSE_LOCAL_KMERGE,
                                    zl.ZL_PLAN_DETERMINISTIC_DQ,
                                    zl.ZL_PLAN_DETERMINISTIC_DQ | zl.ZL_PLAN_FUSE_LOCAL_KMERGE])
 def test_every_plan_passes_the_bounds_dry_run(flags):
@@ -360,3 +368,71 @@ def test_plan_queries_check_their_arguments(lib):
     assert lib.zl_plan_arena_sizes(None, None, None, None, None, None, None) == zl.ZL_ERR_INVALID_ARG
     assert lib.zl_plan_check_bounds(None) == zl.ZL_ERR_INVALID_ARG
     assert lib.zl_plan_worklist(None, 0, 1, 64, 1, 0, None) == zl.ZL_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- caller-chosen merge groups
+def _kv_split_list():
+    # a 512-token sequence (2 heads) as four k-split chunks, beside a whole sequence
+    return [WorkItem(0, 100, 0, 100, 0, 2, 0, 100),
+            WorkItem(100, 512, 0, 512, 0, 2, 0, 128, 1), WorkItem(100, 512, 0, 512, 0, 2, 128, 256, 1),
+            WorkItem(100, 512, 0, 512, 0, 2, 256, 384, 1), WorkItem(100, 512, 0, 512, 0, 2, 384, 512, 1)]
+
+
+def test_explicit_groups_set_membership_and_member_order():
+    items = _kv_split_list()
+    p = zl.zl_plan_worklist_groups(items, 2, 64, 612, [[4, 2], [1, 3]], flags=zl.ZL_PLAN_HOST_ONLY)
+    assert p.n_groups == 2
+    assert p.group(0)[0] == [4, 2] and p.group(1)[0] == [1, 3]
+    # each group has its own final block; members read their group's
+    o0, o1 = p.group(0)[1], p.group(1)[1]
+    assert o0 != o1
+    assert p.item(4).fin_out_offset == p.item(2).fin_out_offset == o0
+    assert p.item(1).fin_out_offset == p.item(3).fin_out_offset == o1
+    p.check_bounds()
+    # the default grouping of the same list: one group in list order
+    d = zl.zl_plan_worklist(items, 2, 64, 612, flags=zl.ZL_PLAN_HOST_ONLY)
+    assert d.n_groups == 1 and d.group(0)[0] == [1, 2, 3, 4]
+    same = zl.zl_plan_worklist_groups(items, 2, 64, 612, [[1, 2, 3, 4]], flags=zl.ZL_PLAN_HOST_ONLY)
+    assert same.tiles(0) == d.tiles(0) and same.group(0) == d.group(0)
+
+
+@pytest.mark.parametrize("groups", [
+    [[1, 2], [3]],               # item 4 in no group
+    [[1, 2], [3, 4], [2]],       # item 2 twice
+    [[0, 1], [2, 3, 4]],         # item 0 is not a k-split item
+    [[1, 2, 3, 4, 5]],           # id out of range
+    [[1, 2], [], [3, 4]],        # empty group
+])
+def test_explicit_groups_reject_malformed_lists(groups):
+    with pytest.raises(zl.ZlError) as e:
+        zl.zl_plan_worklist_groups(_kv_split_list(), 2, 64, 612, groups, flags=zl.ZL_PLAN_HOST_ONLY)
+    assert e.value.status == zl.ZL_ERR_INVALID_ARG
+
+
+def test_explicit_groups_reject_mixed_keys_and_overlap():
+    items = _kv_split_list() + [WorkItem(100, 512, 0, 256, 0, 2, 0, 512, 1)]   # other rows
+    with pytest.raises(zl.ZlError):
+        zl.zl_plan_worklist_groups(items, 2, 64, 612, [[1, 2, 3, 4, 5]], flags=zl.ZL_PLAN_HOST_ONLY)
+    ok = zl.zl_plan_worklist_groups(items, 2, 64, 612, [[1, 2, 3, 4], [5]], flags=zl.ZL_PLAN_HOST_ONLY)
+    assert ok.n_groups == 2
+    over = _kv_split_list() + [WorkItem(100, 512, 0, 512, 0, 2, 64, 192, 1)]    # overlaps chunks 1, 2
+    with pytest.raises(zl.ZlError):
+        zl.zl_plan_worklist_groups(over, 2, 64, 612, [[1, 2, 3, 4, 5]], flags=zl.ZL_PLAN_HOST_ONLY)
+    # the same chunk in a group of its own is a separate problem: accepted
+    ok = zl.zl_plan_worklist_groups(over, 2, 64, 612, [[1, 2, 3, 4], [5]], flags=zl.ZL_PLAN_HOST_ONLY)
+    ok.check_bounds()
+
+
+def test_explicit_groups_bad_pointer_arrays(lib):
+    items = zl._to_c_items(_kv_split_list())
+    h = ctypes.c_void_p()
+    ids = (ctypes.c_int32 * 4)(1, 2, 3, 4)
+    bad_start = (ctypes.c_int32 * 2)(1, 4)
+    assert lib.zl_plan_worklist_groups(items, 5, 2, 64, 612, zl.ZL_PLAN_HOST_ONLY, ids, bad_start, 1,
+                                       ctypes.byref(h)) == zl.ZL_ERR_INVALID_ARG
+    decreasing = (ctypes.c_int32 * 3)(0, 3, 2)
+    assert lib.zl_plan_worklist_groups(items, 5, 2, 64, 612, zl.ZL_PLAN_HOST_ONLY, ids, decreasing, 2,
+                                       ctypes.byref(h)) == zl.ZL_ERR_INVALID_ARG
+    assert lib.zl_plan_worklist_groups(items, 5, 2, 64, 612, zl.ZL_PLAN_HOST_ONLY, None, None, 1,
+                                       ctypes.byref(h)) == zl.ZL_ERR_INVALID_ARG
+    assert h.value is None

@@ -17,21 +17,19 @@ FUSE = zl.ZL_PLAN_FUSE_LOCAL_KMERGE
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("variant", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE])
-def test_fused_edges_all_rows(d, variant):
+def test_fused_edges_all_rows(d):
     # a 3-way k split with an empty, unaligned middle chunk, beside whole and
-    # degenerate items; both forward kernels
+    # degenerate items
     H = 3
     w = Workload(f"edges_d{d}", H, d, 300, tiny_edge_items(H), d ** -0.5)
-    r = Run(w, seed=5, flags=FUSE | variant)
+    r = Run(w, seed=5, flags=FUSE)
     assert r.plan.n_merge_groups == 0 and r.plan.n_groups == 1
     r.check_forward()
 
 
-@pytest.mark.parametrize("variant", [0, zl.ZL_PLAN_FWD_ONE_SUBTILE])
-def test_fused_long_video_sampled_rows(variant):
+def test_fused_long_video_sampled_rows():
     # 8 chunks of a video (lengths / 8) fused into one item of the whole KV range
-    r = Run(scaled(config_long_video(), 8), seed=6, flags=FUSE | variant)
+    r = Run(scaled(config_long_video(), 8), seed=6, flags=FUSE)
     assert r.plan.n_merge_groups == 0
     r.check_forward(sample=1024)
 

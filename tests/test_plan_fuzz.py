@@ -11,8 +11,8 @@ from coalesced_packed_attention_gb300 import zl
 from coalesced_packed_attention_gb300.workloads import WorkItem, merge_groups
 from tests._lib import ensure_library
 
-FLAG_SETS = [0, zl.ZL_PLAN_FWD_ONE_SUBTILE, zl.ZL_PLAN_DETERMINISTIC_DQ, zl.ZL_PLAN_FUSE_LOCAL_KMERGE,
-             zl.ZL_PLAN_FUSE_LOCAL_KMERGE | zl.ZL_PLAN_DETERMINISTIC_DQ | zl.ZL_PLAN_FWD_ONE_SUBTILE]
+FLAG_SETS = [0, zl.ZL_PLAN_DETERMINISTIC_DQ, zl.ZL_PLAN_FUSE_LOCAL_KMERGE,
+             zl.ZL_PLAN_FUSE_LOCAL_KMERGE | zl.ZL_PLAN_DETERMINISTIC_DQ]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -81,7 +81,7 @@ def check_plan(H, d, T, items, flags):
     ft = p.tiles(0)
     assert [t[3] for t in ft] == sorted((t[3] for t in ft), reverse=True)
     if not fused:
-        fb = 128 if flags & zl.ZL_PLAN_FWD_ONE_SUBTILE else 256
+        fb = 256
         want = {(i, h, b) for i, it in enumerate(items) for h in range(it.h_lo, it.h_hi)
                 for b in range(-(-it.nq // fb))}
         got = [(i, h, b) for (i, h, b, _) in ft]

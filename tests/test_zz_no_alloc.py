@@ -6,8 +6,10 @@ start-up.  zl_coalesced_attn_fwd_noalloc serves them: it takes the work list its
 (no zl_plan, whose creation allocates), keeps its tables in a fixed scratch array
 compiled into the library, and launches the same forward kernel.  This test calls it
 through the C ABI twice in a row and checks each result against zl_coalesced_attn_fwd
-on the same inputs, with the tolerances of the other parity tests.  It lives in a file of
-its own, collected last.
+on the same inputs, with the tolerances of the other parity tests; on the tiny list it
+also checks the result against the CPU float64 oracle, and after every call it reads the
+array's status word through zl_noalloc_get_device_status.  It lives in a file of its own,
+collected last.
 """
 import ctypes
 
@@ -17,7 +19,7 @@ import pytest
 from coalesced_packed_attention_gb300 import zl
 from coalesced_packed_attention_gb300.workloads import config_mixed, config_tiny, make_inputs, scaled
 from tests._lib import ensure_library
-from tests.gpu_util import ATOL_LSE, ATOL_O, check
+from tests.gpu_util import ATOL_LSE, ATOL_O, check, oracle_forward
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +33,20 @@ def _entry(lib):
     return fn
 
 
+def _status_entry(lib):
+    fn = lib.zl_noalloc_get_device_status
+    fn.restype = ctypes.c_int32
+    fn.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+    return fn
+
+
+def _device_status(lib, stream):
+    word = ctypes.c_int32(-1)
+    st = _status_entry(lib)(stream, ctypes.byref(word))
+    assert st == zl.ZL_OK, zl.status_string(st)
+    return word.value
+
+
 def _blocks(plan, items, bufs, d):
     """Every item's own O and LSE block, and every merge group's, as numpy arrays."""
     out = []
@@ -42,6 +58,15 @@ def _blocks(plan, items, bufs, d):
         out.append(arena[r.out_offset: r.out_offset + n * d])
         out.append(lse[r.lse_offset: r.lse_offset + n])
     return out
+
+
+def test_noalloc_status_query_before_any_forward():
+    # the query sets up the array's address itself when it is the first call on a device
+    import torch
+    lib = ensure_library()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert _device_status(lib, stream) == zl.ZL_OK
+    assert _status_entry(lib)(stream, None) == zl.ZL_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("make", [config_tiny, lambda: scaled(config_mixed(), 12)], ids=["tiny", "mixed_div12"])
@@ -66,10 +91,18 @@ def test_noalloc_forward_matches_the_plan_forward_on_two_calls(make):
         st = fn(items, len(w.items), H, d, T, q.data_ptr(), k.data_ptr(), v.data_ptr(), out["o"].data_ptr(),
                 out["o_partial"].data_ptr(), out["lse"].data_ptr(), ctypes.c_float(w.scale), stream)
         assert st == zl.ZL_OK, zl.status_string(st)
+        assert _device_status(lib, stream) == zl.ZL_OK  # no bounded wait gave up
         torch.cuda.synchronize()
         got = _blocks(plan, w.items, out, d)
         for j, (g, r) in enumerate(zip(got, ref_blocks)):
             check(f"call{call}.block{j}", g, r, ATOL_LSE if j % 2 else ATOL_O)
+        if w.name.startswith("tiny"):
+            # and against the oracle: every item's own O / LSE (k-split chunks: partials)
+            qn, kn, vn = (x.float().cpu().numpy() for x in (q, k, v))
+            for i, it in enumerate(w.items):
+                O_ref, L_ref = oracle_forward(qn, kn, vn, it, w.scale)
+                check(f"call{call}.item{i}.O", got[2 * i].reshape(O_ref.shape), O_ref, ATOL_O)
+                check(f"call{call}.item{i}.LSE", got[2 * i + 1].reshape(L_ref.shape), L_ref, ATOL_LSE)
 
 
 def test_noalloc_rejects_a_list_beyond_its_scratch():
