@@ -4,46 +4,15 @@ h-split, k-split with the merged global LSE (partial dQ)."""
 import numpy as np
 import pytest
 
-import oracle
-from coalesced_packed_attention_gb300.workloads import Workload, config_training, merge_groups, scaled
-from tests.gpu_util import ATOL_GRAD_STRUCTURED, ATOL_O, Run, check, sample_rows, tiny_edge_items
+from coalesced_packed_attention_gb300.workloads import Workload, config_training, scaled
+from tests.gpu_util import Run, check_gradients, oracle_pairs, tiny_edge_items
 
 pytestmark = pytest.mark.gpu
 
 
-def final_reference(r, rows_of=None):
-    """Oracle final O and LSE (all rows) of every item: its own, or its group's merge."""
-    fin = {}
-    parts = {}
-    for i, it in enumerate(r.items):
-        parts[i] = oracle.forward(r.q, r.k, r.v, it, r.scale)
-    for g in merge_groups(r.items):
-        m = oracle.merge([parts[i] for i in g])
-        for i in g:
-            fin[i] = m
-    for i in range(len(r.items)):
-        fin.setdefault(i, parts[i])
-    return fin
-
-
 def check_backward(r, kv_sample=None, q_sample=None, seed=0):
-    fin = final_reference(r)
-    tol = ATOL_GRAD_STRUCTURED if r.relative else ATOL_O
-    for i, it in enumerate(r.items):
-        if it.nq == 0 or it.nh == 0:
-            continue
-        O, L = fin[i]
-        s = it.seq_offset
-        do_all = r.do[s + it.q_lo: s + it.q_hi, it.h_lo:it.h_hi]
-        rows = np.arange(it.nq) if q_sample is None else sample_rows(it.nq, seed + i, q_sample)
-        dQ_ref = oracle.backward_dq(r.q, r.k, r.v, do_all[rows], O[rows], L[:, rows], it, r.scale, it.q_lo + rows)
-        check(f"item{i}.dQ", r.grad(i, "dq")[rows], dQ_ref, tol, relative=r.relative)
-        if it.nkv == 0:
-            continue
-        kv = np.arange(it.nkv) if kv_sample is None else sample_rows(it.nkv, seed + 7 * i, kv_sample)
-        dK_ref, dV_ref = oracle.backward_dkdv(r.q, r.k, r.v, do_all, O, L, it, r.scale, it.kv_lo + kv)
-        check(f"item{i}.dK", r.grad(i, "dk")[kv], dK_ref, tol, relative=r.relative)
-        check(f"item{i}.dV", r.grad(i, "dv")[kv], dV_ref, tol, relative=r.relative)
+    _, final = oracle_pairs(r)
+    check_gradients(r, final, q_sample=q_sample, kv_sample=kv_sample, seed=seed)
 
 
 def test_training_list_scaled_all_rows():
