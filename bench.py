@@ -33,7 +33,7 @@ import numpy as np  # noqa: E402
 METRIC = "coalesced attn TFLOP/s (fwd+bwd training step)"
 UNIT = "TFLOP/s"
 KERNEL_SOURCES = {"zl_bwd_main": "coalesced_packed_attention_gb300/csrc/zl_bwd.cu",
-                  "zl_coalesced_attn_fwd": "coalesced_packed_attention_gb300/csrc/zl_fwd.cu"}
+                  "zl_coalesced_attn_fwd": "coalesced_packed_attention_gb300/csrc/zl_fwd2.cu"}
 
 
 def dist_env():
@@ -222,8 +222,7 @@ def run_gpu(args):
 
     t_plan = time.perf_counter()
     plan = zl.zl_plan_worklist(work.items, H, d, T,
-                               (zl.ZL_PLAN_FWD_ONE_SUBTILE if args.fwd_one_subtile else 0)
-                               | (zl.ZL_PLAN_FUSE_LOCAL_KMERGE if args.fuse_kmerge else 0)
+                               (zl.ZL_PLAN_FUSE_LOCAL_KMERGE if args.fuse_kmerge else 0)
                                | (zl.ZL_PLAN_DETERMINISTIC_DQ if args.deterministic else 0))
     t_plan = time.perf_counter() - t_plan
 
@@ -348,9 +347,22 @@ def run_gpu(args):
         b.record(s_comp)
         torch.cuda.synchronize(dev)
         e_val, e_ms = aggregate(torch.tensor([a.elapsed_time(b)], device=dev), ws, F_step, n_e2e)
+        # one call at a time: a step's uploads, its launches and its downloads, then the
+        # host waits for the results before the next call (host clock, host to host)
+        single = []
+        for _ in range(max(3, min(args.steps, 6))):
+            t_a = time.perf_counter()
+            e2e_step(0)
+            torch.cuda.synchronize(dev)
+            single.append(time.perf_counter() - t_a)
+        s_ms = 1e3 * float(np.median(single))
         e2e = {"value": e_val, "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "pipelined": "2 buffer sets; every input's H2D and every output's D2H on its own stream"}
+               "pipelined": ("throughput of a stream of steps: 2 device buffer sets, so one step's uploads and "
+                             "the previous step's downloads run under the current step's kernels; every "
+                             "input's H2D and every output's D2H on its own stream"),
+               "single_call": {"value": F_step / (s_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": s_ms,
+                               "note": "one call's host-to-host time (uploads, step, downloads, host sync)"}}
         del sets
 
     peaks, peak_kind = measured_peaks()
@@ -360,17 +372,29 @@ def run_gpu(args):
     # dominant kernel: the tcgen05 backward (largest share of the step)
     bwd_tf = F_bwd / (bwd_ms * 1e-3) / 1e12
     fwd_tf = F_fwd / (fwd_ms * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops_sustained"])
+    # both kernels are event-timed inside a step of ~50 ms (under a second of timed steps):
+    # the burst figure of the measured cuBLAS bf16 GEMM is the matching denominator
+    peak = float(peaks["bf16_tflops"])
+    clocks = summarize_clocks(clock_lines, dev.index or 0)
+    # the same rates at the maximum SM clock, from the clocks sampled in the timed region
+    clk = (clocks["sm_max_mhz"] / clocks["sm_mhz"]) if clocks.get("sm_mhz") and clocks.get("sm_max_mhz") else None
     traffic = recorded_traffic("zl_bwd_main")
     # algorithmic bytes of the HBM-bound kernels
     merge_bytes = 0
-    grp_rows = 0
     for g in range(plan.n_groups):
         members, _, _ = plan.group(g)
         it = work.items[members[0]]
-        grp_rows += len(members) * it.nq * it.nh
         merge_bytes += len(members) * it.nq * it.nh * (4 * d + 4) + it.nq * it.nh * (2 * d + 4)
     pre_bytes = sum(it.nq * it.nh * (2 * d + 2 * d + 4 + 4 * d) for it in work.items)
+    fin_bytes = sum(it.nq * it.nh * 8 * d for it in work.items)
+    hbm = float(peaks["hbm_gbs"])
+    extra = {}
+    if rank == 0 and not args.no_extras:
+        # the co-location check and the forward-only lists, after the timed region
+        extra["additivity"] = additivity_numbers(work, q, k, v, do_tok, dev, stream, 3)
+        del bufs, d_o
+        torch.cuda.empty_cache()
+        extra["forward_configs"] = forward_config_numbers(dev, stream, 5, 2, peak)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -388,15 +412,22 @@ def run_gpu(args):
                         "max": float(step_each.max())},
             "merge_gbs": merge_bytes / (merge_ms * 1e-3) / 1e9 if merge_ms > 0 and plan.n_merge_groups else None,
             "bwd_preprocess_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9 if pre_ms > 0 else None,
+            "bwd_finalize_gbs": fin_bytes / (fin_ms * 1e-3) / 1e9 if fin_ms > 0 else None,
+            "hbm_peak_gbs": hbm,
             "plan_ms": t_plan * 1e3,
             "roofline": {"kernel": "zl_bwd_main (tcgen05 backward)", "bound": "tensor", "achieved": bwd_tf,
-                         "peak": peak, "peak_kind": f"{peak_kind} bf16 sustained", "unit": "TFLOP/s",
+                         "peak": peak, "peak_kind": f"{peak_kind} bf16 burst", "unit": "TFLOP/s",
                          "frac": bwd_tf / peak, "traffic": traffic,
-                         "fwd": {"achieved": fwd_tf, "frac": fwd_tf / peak}},
+                         "clock_adjusted": ({"achieved": bwd_tf * clk, "frac": bwd_tf * clk / peak,
+                                             "sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"]}
+                                            if clk else None),
+                         "fwd": {"achieved": fwd_tf, "frac": fwd_tf / peak,
+                                 "clock_adjusted_frac": fwd_tf * clk / peak if clk else None}},
             # forward, merge (unless every group is fused), row sums, backward, finalize
             "gpu_launches": (4 + (1 if plan.n_merge_groups else 0)) * args.steps,
-            "clocks": summarize_clocks(clock_lines, dev.index or 0),
+            "clocks": clocks,
         }
+        line.update(extra)
         if e2e is not None:
             line["e2e"] = e2e
         if ws == 1 and not args.no_cpu_baseline:
@@ -408,29 +439,21 @@ def run_gpu(args):
         torch.distributed.destroy_process_group()
 
 
-def run_additivity(args):
+def additivity_numbers(work, q, k, v, do_tok, dev, stream, reps):
     """Co-location check of the additive time model: every work item timed alone (a plan
     holding only that item, same inputs) against the coalesced launch of the whole list,
     forward + merge + backward.  The pages' profiler prices each (bucket, configuration)
     pair separately and takes a rank's time as their sum, assuming that co-locating whole
     sequences with shards costs nothing extra (pith.science review, "Load-bearing premise").
     ratio = coalesced / sum of solo times: 1.0 means additive, < 1 means co-location helps
-    (the persistent launch fills SMs that a lone item would leave idle)."""
+    (the persistent launch fills SMs that a lone item would leave idle).  Each plan runs
+    one untimed step, then `reps` steps between two events; the median of three such
+    rounds is kept."""
     import torch
     from coalesced_packed_attention_gb300 import zl
-    from coalesced_packed_attention_gb300.workloads import config_training, make_inputs
-
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    work = config_training()
-    if args.scale > 1:
-        from coalesced_packed_attention_gb300.workloads import scaled
-        work = scaled(work, args.scale)
     H, d, T, scale = work.n_heads, work.head_dim, work.total_tokens, work.scale
-    q, k, v, do_tok = make_inputs(T, H, d, seed=0, with_grad_output=True, device=str(dev))
-    stream = torch.cuda.current_stream(dev)
 
-    def timed(items, reps):
+    def timed(items):
         plan = zl.zl_plan_worklist(items, H, d, T)
         d_o = dO_arena(plan, type(work)(work.name, H, d, T, list(items), scale), do_tok, dev)
         bufs = zl.allocate(plan, dev, backward=True)
@@ -440,68 +463,113 @@ def run_additivity(args):
             zl.zl_merge_partials(plan, bufs["o_partial"], bufs["lse"], bufs["o"], bufs["lse"], stream)
             zl.zl_coalesced_attn_bwd(plan, q, k, v, bufs["o"], d_o, bufs["lse"], bufs["dq"], bufs["dk"], bufs["dv"],
                                      bufs["workspace"], scale, stream)
-        for _ in range(2):
-            step()
+        step()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        a.record(stream)
-        for _ in range(reps):
-            step()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        return a.elapsed_time(b) / reps
+        rounds = []
+        for _ in range(3):
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            for _ in range(reps):
+                step()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            rounds.append(a.elapsed_time(b) / reps)
+        if zl.zl_get_device_status(plan, stream) != 0:
+            raise RuntimeError("device status in the co-location check")
+        del bufs, d_o
+        plan.destroy()
+        return float(np.median(rounds))
 
-    coalesced = timed(work.items, args.steps)
-    solo = [timed([it], max(1, args.steps // 2)) for it in work.items]
-    line = {"additivity": {
-        "workload": work.name, "coalesced_ms": coalesced, "sum_solo_ms": float(sum(solo)),
-        "ratio": coalesced / float(sum(solo)),
-        "items": [{"label": lab, "solo_ms": s, "fwd_tflop": it.fwd_flops(d) / 1e12}
-                  for lab, s, it in zip(work.labels, solo, work.items)]}}
-    print(json.dumps(line), flush=True)
+    coalesced = timed(work.items)
+    solo = [timed([it]) for it in work.items]
+    return {"workload": work.name, "coalesced_ms": coalesced, "sum_solo_ms": float(sum(solo)),
+            "ratio": coalesced / float(sum(solo)), "reps": reps,
+            "items": [{"label": lab, "solo_ms": s, "fwd_tflop": it.fwd_flops(d) / 1e12}
+                      for lab, s, it in zip(work.labels, solo, work.items)]}
 
 
-def run_forward_configs(args):
-    """Forward (+ merge) TFLOP/s of the forward-only work lists: 64 whole images
-    (48 x 256, 12 x 1024, 4 x 4096 tokens), the mixed list (16 x 1024-token images with
-    q/h/k shards of a 32760-token video and the complementary k chunk), and the
-    147600-token video as 8 k chunks beside 8 x 4096-token images.  Median of the steps;
-    one JSON line per list."""
+def run_additivity(args):
+    """--additivity: the co-location check alone (its own JSON line)."""
     import torch
     from coalesced_packed_attention_gb300 import zl
-    from coalesced_packed_attention_gb300.workloads import (config_images, config_long_video, config_mixed,
-                                                            make_inputs)
+    from coalesced_packed_attention_gb300.workloads import config_training, make_inputs
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    zl.load_library()
+    work = config_training()
+    if args.scale > 1:
+        from coalesced_packed_attention_gb300.workloads import scaled
+        work = scaled(work, args.scale)
+    q, k, v, do_tok = make_inputs(work.total_tokens, work.n_heads, work.head_dim, seed=0, with_grad_output=True,
+                                  device=str(dev))
     stream = torch.cuda.current_stream(dev)
-    for work in (config_images(), config_mixed(), config_long_video()):
+    print(json.dumps({"additivity": additivity_numbers(work, q, k, v, do_tok, dev, stream, max(2, args.steps))}),
+          flush=True)
+
+
+def forward_config_numbers(dev, stream, steps, warmup, peak):
+    """Forward (+ merge) TFLOP/s of the forward-only work lists: 64 whole images
+    (48 x 256, 12 x 1024, 4 x 4096 tokens), and the 147600-token video as 8 k chunks
+    beside 8 x 4096-token images, merged (fp32 partials + merge launch) and with the
+    k-split group fused into the forward (ZL_PLAN_FUSE_LOCAL_KMERGE).  Median of the
+    steps; the merge's GB/s from its algorithmic bytes."""
+    import torch
+    from coalesced_packed_attention_gb300 import zl
+    from coalesced_packed_attention_gb300.workloads import config_images, config_long_video, make_inputs
+
+    out = []
+    for work, flags, tag in ((config_images(), 0, "merged"), (config_long_video(), 0, "merged"),
+                             (config_long_video(), zl.ZL_PLAN_FUSE_LOCAL_KMERGE, "fused")):
         H, d, T, scale = work.n_heads, work.head_dim, work.total_tokens, work.scale
         q, k, v = make_inputs(T, H, d, seed=0, device=str(dev))[:3]
-        plan = zl.zl_plan_worklist(work.items, H, d, T)
+        plan = zl.zl_plan_worklist(work.items, H, d, T, flags)
         bufs = zl.allocate(plan, dev)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         times = []
-        for s in range(args.warmup + args.steps):
+        for s_ in range(warmup + steps):
             ev[0].record(stream)
             zl.zl_coalesced_attn_fwd(plan, q, k, v, bufs["o"], bufs["o_partial"], bufs["lse"], scale, stream)
             ev[1].record(stream)
             zl.zl_merge_partials(plan, bufs["o_partial"], bufs["lse"], bufs["o"], bufs["lse"], stream)
             ev[2].record(stream)
             torch.cuda.synchronize(dev)
-            if s >= args.warmup:
+            if s_ >= warmup:
                 times.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
         if zl.zl_get_device_status(plan, stream) != 0:
             raise RuntimeError(f"device status after {work.name}")
         f_ms = float(np.median([a for a, _ in times]))
         m_ms = float(np.median([b for _, b in times]))
         F = work.fwd_flops()
-        print(json.dumps({"forward_config": {
-            "workload": work.name, "fwd_tflop": F / 1e12, "fwd_ms": f_ms, "merge_ms": m_ms,
-            "tflops_fwd_plus_merge": F / ((f_ms + m_ms) * 1e-3) / 1e12, "tflops_fwd": F / (f_ms * 1e-3) / 1e12,
-            "fwd_tiles": plan.n_fwd_tiles}}), flush=True)
+        merge_bytes = 0
+        for g in range(plan.n_groups):
+            members, _, _ = plan.group(g)
+            it = work.items[members[0]]
+            if plan.n_merge_groups:
+                merge_bytes += len(members) * it.nq * it.nh * (4 * d + 4) + it.nq * it.nh * (2 * d + 4)
+        tf = F / ((f_ms + m_ms) * 1e-3) / 1e12
+        out.append({"workload": work.name, "kmerge": tag if plan.n_groups else None, "fwd_tflop": F / 1e12,
+                    "fwd_ms": f_ms, "merge_ms": m_ms, "tflops_fwd_plus_merge": tf,
+                    "tflops_fwd": F / (f_ms * 1e-3) / 1e12, "frac_fwd_plus_merge": tf / peak,
+                    "merge_gbs": merge_bytes / (m_ms * 1e-3) / 1e9 if merge_bytes and m_ms > 0 else None,
+                    "fwd_tiles": plan.n_fwd_tiles})
         del bufs, q, k, v
         plan.destroy()
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_forward_configs(args):
+    """--forward-configs: the forward-only lists alone (one JSON line)."""
+    import torch
+    from coalesced_packed_attention_gb300 import zl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    zl.load_library()
+    peaks, _ = measured_peaks()
+    print(json.dumps({"forward_configs": forward_config_numbers(dev, torch.cuda.current_stream(dev), args.steps,
+                                                                args.warmup, float(peaks["bf16_tflops"]))}),
+          flush=True)
 
 
 def run_kmerge_compare(args):
@@ -614,10 +682,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the co-location check and the forward-only lists after the timed region")
     ap.add_argument("--scale", type=int, default=1,
                     help="divide every length of the list by this factor (profiler captures only)")
-    ap.add_argument("--fwd-one-subtile", action="store_true",
-                    help="use the 128-row single-warpgroup forward variant")
     ap.add_argument("--additivity", action="store_true",
                     help="time every work item alone and the coalesced list (co-location check)")
     ap.add_argument("--fuse-kmerge", action="store_true",
