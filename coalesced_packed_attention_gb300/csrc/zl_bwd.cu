@@ -17,22 +17,23 @@
 //   dV  += P^T dO_i     (TMEM x SMEM, dO read MN-major)
 //   dQ_i = dS K         (SMEM x SMEM -> TMEM R1; both operands MN-major)
 //   dK  += dS^T Q_i     (SMEM x SMEM; dS^T read K-major, Q MN-major)
-//   the dQ warpgroup (thread = query row) reads dQ_i out of TMEM and adds it to the fp32
-//   accumulator with 16-byte vector reductions issued straight from registers; the scale
-//   is applied once when dQ is finalised.
+//   the dQ warpgroup (thread = query row) reads dQ_i out of TMEM, stages it through shared
+//   memory 16 KB at a time and hands each chunk to the bulk-copy engine as one reduce-add
+//   into the fp32 accumulator; the scale is applied once when dQ is finalised.
 // The tensor pipe runs dP^T_i, dV_i, S^T_{i+1}, dQ_i, dK_i: R0 is free once dV_i has
 // read P^T and R1 once the warpgroups have read dP^T_i, so the softmax warpgroups form
 // P_{i+1} while dQ_i and dK_i run and dQ_i drains.  The drain has warps of its own
-// because an SM hands reductions to L2 at roughly 45 GB/s whichever unit issues them
-// (measured on GB300 for TMA tensor reduce-adds, bulk reduce-adds and vector `red`
-// alike): the 64 KB of one block's dQ take about as long as the block's five products,
-// so they must overlap everything else.  The drain paces its reductions over the
-// block period: issued in a burst they fill each sub-partition's memory-instruction
-// queue and hold up the TMEM loads, MMA issues and TMA issues of the warps beside them.
+// because an SM hands reductions to L2 at only some 30-45 GB/s, whichever unit issues
+// them: the 64 KB of one block's dQ take about as long as the block's five products, so
+// they must overlap everything else.  Bulk reduce-adds from shared memory keep them out
+// of the sub-partitions' memory-instruction queues, where vector `red` instructions
+// (paced or not) held up the TMEM loads, MMA issues and TMA issues of the warps beside
+// them; the dQ reduction rate is what bounds the kernel on long items.
 // Ordered dQ (plan flag ZL_PLAN_DETERMINISTIC_DQ; a separate instantiation, so the
 // default kernel carries none of it): the order in which CTAs reach a query block
 // decides the order of the fp32 additions, so by default dQ may change in its last bits
-// between runs.  With the flag, each drain warp waits before adding its 32 rows of a
+// between runs.  With the flag, the drain adds with vector reductions from registers,
+// and each drain warp waits before adding its 32 rows of a
 // block until that slice's turn counter (workspace) equals its KV-block index, and
 // passes the turn on (index + 1, after a fence) when it reaches its next block, by
 // which time most of those reductions have landed (handing it over right after the
@@ -42,7 +43,8 @@
 // are claimed in ascending order and far apart: waits are rare and only ever on tiles
 // claimed earlier (held by running CTAs), which rules out a cycle of waits.
 // TMEM (512 columns): R0 [0,128) S^T / P^T, R1 [128,256) dP^T / dQ, dV [256,256+d),
-// dK [384,384+d).
+// dK [384,384+d).  Shared memory: K, V, Q (2 stages), dO (1 stage: free once dV has read
+// it), dS^T, and two 16 KB dQ staging buffers.
 // Warps: 0-7 softmax (two warpgroups), 8-11 dQ drain, 12 TMA producer, 13 MMA issuer,
 // 14-15 idle.  The block is launched with 128 registers per thread (16 warps: four per
 // SM sub-partition, 16K registers each) and the warpgroups then trade registers with
@@ -51,7 +53,6 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include "zl_exp2.cuh"
 #include "zl_internal.h"
 #include "zl_kernels.h"
 #include "zl_ptx.cuh"
@@ -67,33 +68,18 @@ struct BwdLayout {
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;             // 2 stages
-  static constexpr int kDO = kQ + 2 * kTile;        // 2 stages
-  static constexpr int kDS = kDO + 2 * kTile;       // [128 kv][128 q] bf16, two 128-byte-swizzled boxes
-  static constexpr int kLD = kDS + 2 * kBox;        // [2 block parities] LSE*log2(e) and D of a block's 128 queries
+  static constexpr int kDO = kQ + 2 * kTile;        // 1 stage (free once dV has read it)
+  static constexpr int kDS = kDO + kTile;           // [128 kv][128 q] bf16, two 128-byte-swizzled boxes
+  static constexpr int kStageBytes = 128 * 32 * 4;  // one 32-column chunk of a block's dQ, fp32
+  static constexpr int kStage = kDS + 2 * kBox;     // 2 staging buffers of the dQ drain
+  static constexpr int kLD = kStage + 2 * kStageBytes;  // [2 block parities] LSE*log2(e) and D of a block's 128 queries
   static constexpr int kBar = kLD + 2 * 2 * 128 * 4;
-  static constexpr int kNumBars = 21;
+  static constexpr int kNumBars = 25;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 64;
 };
 
 constexpr float kLog2eB = 1.44269504088896340736f;
-// Query pairs (bit e: queries 2e, 2e+1 of each 32-query half of a warpgroup's columns)
-// whose P exponents are computed on the FMA pipe (exp2_poly2) rather than the
-// special-function unit: every other pair (measured on the training list: 1.4 % faster
-// than all on the special-function unit; in the forward the same split was slower).
-#ifndef ZL_BWD_POLY_PAIRS
-#define ZL_BWD_POLY_PAIRS 0x5555u
-#endif
-constexpr uint32_t kPolyPairs = ZL_BWD_POLY_PAIRS;
-// dQ drain pacing: a warp's reductions of one block are spread over the previous block
-// period times 8 / ZL_DRAIN_SPREAD_EIGHTHS, or issued ZL_DRAIN_PACE_FIXED cycles apart
-// when that is set (> 0).
-#ifndef ZL_DRAIN_SPREAD_EIGHTHS
-#define ZL_DRAIN_SPREAD_EIGHTHS 9
-#endif
-#ifndef ZL_DRAIN_PACE_FIXED
-#define ZL_DRAIN_PACE_FIXED 0
-#endif
 constexpr float kInfB = __builtin_huge_valf();
 
 __device__ __forceinline__ void rec_err(int32_t* status, volatile int* abort_flag, int code) {
@@ -129,6 +115,19 @@ __device__ __forceinline__ void red_add_v4(float* addr, uint32_t a, uint32_t b, 
                "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
                : "memory");
 }
+
+// Bulk (1-D) reduce-add of `bytes` bytes of fp32 from shared memory into global memory
+// by the bulk-copy engine, tracked by this thread's bulk groups.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most one of this thread's bulk groups still has to read its source
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// wait until all of this thread's bulk groups are complete (their writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Tiles of one (item, head) walk the query blocks starting at different blocks, so
 // CTAs running side by side add into different dQ rows instead of contending on one.
@@ -211,7 +210,8 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
   uint64_t* kv_full = bar + 0;
   uint64_t* kv_empty = bar + 1;
   uint64_t* q_full = bar + 2;     // [2]
-  uint64_t* do_full = bar + 4;    // [2]
+  uint64_t* do_full = bar + 4;    // dO of the block in shared memory
+  uint64_t* do_empty = bar + 5;   // dV (the last reader of dO) complete
   uint64_t* q_empty = bar + 6;    // [2]
   uint64_t* s_full = bar + 8;     // S^T of the block in TMEM R0
   uint64_t* ds_ready = bar + 9;   // dS^T in shared memory, dP^T read out of R1 (256 arrivals)
@@ -224,6 +224,8 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
   uint64_t* ld_full = bar + 18;   // LSE / D of a query block staged in shared memory
   uint64_t* p_ready = bar + 19;   // P^T in TMEM R0 (256 arrivals): the dV product may start
   uint64_t* dp_full = bar + 20;   // dP^T of the block in TMEM R1
+  uint64_t* stage_full = bar + 21;  // [2] a dQ chunk written to staging buffer b (128 arrivals)
+  uint64_t* stage_free = bar + 23;  // [2] the bulk reduce-add of buffer b has read it
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   uint32_t* tmem_slot = misc;
   volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(misc + 2);
@@ -240,11 +242,14 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
     mbar_init(kv_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(q_full + i, 1);
-      mbar_init(do_full + i, 1);
       mbar_init(q_empty + i, 1);
+      mbar_init(stage_full + i, 128);
+      mbar_init(stage_free + i, 1);
       mbar_init(tile_full + i, 1);
       mbar_init(tile_empty + i, 1 + 8 + 4);
     }
+    mbar_init(do_full, 1);
+    mbar_init(do_empty, 1);
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
@@ -321,9 +326,11 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           for (int c = 0; c < D / 64; ++c)
             tma_load_3d(sQ + st * L::kTile + c * L::kBox, &tm_q, q_full + st, 64 * c, tl.head,
                         (int)it.seq_offset + it.q_lo + ib * kBlockM);
-          mbar_arrive_expect_tx(do_full + st, L::kTile);
+          // one dO slot: block qit's dO waits until dV of block qit - 1 has read the slot
+          if (!bwait(do_empty, (qit & 1) ^ 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(do_full, L::kTile);
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sDO + st * L::kTile + c * L::kBox, tm_do, do_full + st, 64 * c, hl, ib * kBlockM);
+            tma_load_3d(sDO + c * L::kBox, tm_do, do_full, 64 * c, hl, ib * kBlockM);
           ++qit;
         }
       }
@@ -381,14 +388,14 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         tc_fence_after();
         issue_s(qit & 1);
         for (int is = 0; is < nqb; ++is) {
-          const uint32_t st = qit & 1, ph = (qit >> 1) & 1;
-          if (!wait_w(do_full + st, ph)) { ok = false; break; }
+          const uint32_t st = qit & 1;
+          if (!wait_w(do_full, qit & 1)) { ok = false; break; }
           if (nblocks > 0 && !wait_w(dq_empty, (nblocks - 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-            mma_ss_w(tR1, dsc(kV, off), dsc(kDO, st * L::kTile + off), kIdSq, kk > 0);
+            mma_ss_w(tR1, dsc(kV, off), dsc(kDO, off), kIdSq, kk > 0);
           }
           mma_commit_w(dp_full);
           // dV += P^T dO as soon as P^T is in TMEM (the warpgroup then forms dS^T)
@@ -396,8 +403,8 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // K = 128 queries
-            mma_ts_w(tdV, tR0 + pcol(kk), dsc(mDO, st * L::kTile + kk * 2048), kIdKV,
-                     (is > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_w(tdV, tR0 + pcol(kk), dsc(mDO, kk * 2048), kIdKV, (is > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_w(do_empty);  // the producer may load the next block's dO
           if (is + 1 < nqb) {
             // S^T of the next block as soon as dV has read P^T out of R0 (one thread's
             // products run in issue order): the softmax warpgroups start on it while
@@ -436,22 +443,15 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ drain warpgroup
     // Thread t owns query row t of the block (TMEM lane t); for head-dim column group g
-    // (4 floats) the warp's 32 rows are 512 contiguous bytes of the tiled accumulator.
+    // (4 floats) the warp's 32 rows are 512 contiguous bytes of the tiled accumulator, and
+    // a 32-column chunk of the block (8 groups x 128 rows) is 16 KB contiguous.
     regs_to<kRegsDrain>();
     constexpr int kChunks = D / 32;  // 32-column TMEM loads per row
-    constexpr int kReds = kChunks * 8;  // 16-byte reductions per row
-    // clock cycles between two reductions of a warp: the previous block period spread
-    // over slightly more than a block's reductions, within these bounds.  Ordered adds
-    // are not paced: there a block's reductions stand between the turn and the tile
-    // that waits for it, so they go out at once (measured on the training list: 1.15x
-    // faster than pacing at the lower bound, 1.4x faster than pacing by the period,
-    // which includes the turn waits and so slows the successors in turn).
-    constexpr long long kPaceMin = 48, kPaceMax = 160;
-    constexpr int kSpread = kReds * ZL_DRAIN_SPREAD_EIGHTHS / 8;
+    constexpr bool kBulk = !kOrdered;
     const int t = threadIdx.x & 127;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    uint32_t tile_it = 0, nblocks = 0;
-    long long t_prev = 0;
+    const uint32_t aStage = smem_u32(smem + L::kStage);
+    uint32_t tile_it = 0, nblocks = 0, sit = 0;  // sit: chunks staged so far
     for (;;) {
       const uint32_t slot = tile_it & 1;
       if (!__all_sync(0xffffffffu, bwait(tile_full + slot, (tile_it >> 1) & 1, abort_flag, p.wait_limit, p.status))) break;
@@ -464,7 +464,8 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
       const DevItem it = p.items[tl.item];
       const int nq = it.q_hi - it.q_lo;
       const int nqb = (nq + kBlockM - 1) / kBlockM;
-      float* acc = p.ws_dq + it.ws_dq_offset + (int64_t)(tl.head - it.h_lo) * nqb * (kBlockM * D) + t * 4;
+      float* acc_hd = p.ws_dq + it.ws_dq_offset + (int64_t)(tl.head - it.h_lo) * nqb * (kBlockM * D);
+      float* acc = acc_hd + t * 4;
       // ordered adds: this warp's 32-row slice of accumulator block ib has turn counter
       // turns[4 (block) + warp slice]; KV tile b adds when the counter reads b.  A
       // block's turn is passed on at the next block (or the end of the tile), after a
@@ -484,12 +485,6 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         const int ib = first_block(is, start, nqb);
         if (!__all_sync(0xffffffffu, bwait(dq_full, nblocks & 1, abort_flag, p.wait_limit, p.status))) { ok = false; break; }
         tc_fence_after();
-        const long long t_full = clock64();
-        long long pace = t_prev > 0 ? (t_full - t_prev) / kSpread : kPaceMin;
-        pace = pace < kPaceMin ? kPaceMin : (pace > kPaceMax ? kPaceMax : pace);
-        if constexpr (ZL_DRAIN_PACE_FIXED > 0) pace = ZL_DRAIN_PACE_FIXED;
-        if constexpr (kOrdered) pace = 0;
-        t_prev = t_full;
         float* dst = acc + (int64_t)ib * (kBlockM * D);
         const bool row_ok = ib * kBlockM + t < nq;  // rows past the item hold dS = 0
         // all of the row first: TMEM R1 is released before any reduction is issued
@@ -499,6 +494,39 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(dq_empty);  // the next block's dP^T may overwrite R1
+        if constexpr (kBulk) {
+          // chunk c (columns 32c..32c+31) of block ib is 16 KB contiguous in the tiled
+          // accumulator, [8 column groups][128 rows][4]: each thread writes its row's 8
+          // groups into a staging buffer of the same layout, and one thread issues the
+          // chunk's bulk reduce-add once all 128 rows are in; a buffer is refilled once
+          // the engine has read it (two buffers, so one chunk is staged while the
+          // previous one is read)
+          float* blk = acc_hd + (int64_t)ib * (kBlockM * D);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            const uint32_t b = sit & 1, use = sit >> 1;
+            if (!__all_sync(0xffffffffu, bwait(stage_free + b, (use & 1) ^ 1, abort_flag, p.wait_limit, p.status))) {
+              ok = false;
+              break;
+            }
+            const uint32_t sb = aStage + b * L::kStageBytes;
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              st_shared_v4(sb + (g * kBlockM + t) * 16, u[c][4 * g], u[c][4 * g + 1], u[c][4 * g + 2], u[c][4 * g + 3]);
+            fence_proxy_async_smem();
+            mbar_arrive(stage_full + b);
+            if (warp == 8 && lane == 0 && bwait(stage_full + b, use & 1, abort_flag, p.wait_limit, p.status)) {
+              bulk_reduce_add_f32(blk + c * (32 * kBlockM), sb, L::kStageBytes);
+              bulk_commit();
+              bulk_wait_read_1();  // the other buffer's reduce-add has read it
+              if (sit > 0) mbar_arrive(stage_free + (b ^ 1));
+            }
+            ++sit;
+          }
+          if (!ok) break;
+          ++nblocks;
+          continue;
+        }
         if constexpr (kOrdered) {
           if (pending >= 0) pass_turn(pending);
           bool mine = true;
@@ -508,17 +536,12 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           pending = ib;
         }
         if (row_ok) {
-          long long t_next = clock64();
 #pragma unroll
           for (int c = 0; c < kChunks; ++c)
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              while (clock64() < t_next) {
-              }
+            for (int g = 0; g < 8; ++g)
               red_add_v4(dst + (8 * c + g) * (4 * kBlockM), u[c][4 * g], u[c][4 * g + 1], u[c][4 * g + 2],
                          u[c][4 * g + 3]);
-              t_next += pace;
-            }
         }
         ++nblocks;
       }
@@ -527,6 +550,8 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         if (pending >= 0) pass_turn(pending);
       }
     }
+    // the bulk reduce-adds this thread issued are complete before the kernel ends
+    if (kBulk && warp == 8 && lane == 0) bulk_wait_all();
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     // Two warpgroups share the TMEM lanes (lane = KV row) and split the columns:
@@ -597,25 +622,15 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           // exponent arguments two queries per instruction (the staged LSE is negated)
           const float2 sl2v = make_float2(sl2, sl2);
           const float2* nl2 = reinterpret_cast<const float2*>(sLSE + qc0);
-          // the pairs of kPolyPairs on the FMA pipe (exp2_poly2), the rest on the
-          // special-function unit; rows past the KV chunk get an exact 0
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float2 x0 = fma2(make_float2(__uint_as_float(u0[2 * e]), __uint_as_float(u0[2 * e + 1])), sl2v, nl2[e]);
             const float2 x1 =
                 fma2(make_float2(__uint_as_float(u1[2 * e]), __uint_as_float(u1[2 * e + 1])), sl2v, nl2[16 + e]);
-            float2 p0, p1;
-            if ((kPolyPairs >> e) & 1u) {
-              p0 = exp2_poly2<3>(x0);
-              p1 = exp2_poly2<3>(x1);
-            } else {
-              p0 = make_float2(ex2(x0.x), ex2(x0.y));
-              p1 = make_float2(ex2(x1.x), ex2(x1.y));
-            }
-            pr[2 * e] = kv_ok ? p0.x : 0.f;
-            pr[2 * e + 1] = kv_ok ? p0.y : 0.f;
-            pr[32 + 2 * e] = kv_ok ? p1.x : 0.f;
-            pr[32 + 2 * e + 1] = kv_ok ? p1.y : 0.f;
+            pr[2 * e] = kv_ok ? ex2(x0.x) : 0.f;
+            pr[2 * e + 1] = kv_ok ? ex2(x0.y) : 0.f;
+            pr[32 + 2 * e] = kv_ok ? ex2(x1.x) : 0.f;
+            pr[32 + 2 * e + 1] = kv_ok ? ex2(x1.y) : 0.f;
           }
         }
         // P^T (bf16) over this warpgroup's S^T columns, already read: dV may start now
