@@ -357,6 +357,7 @@ def test_plan_queries_check_their_arguments(lib):
     I64, I32 = ctypes.c_int64, ctypes.c_int32
     c = I64()
     assert lib.zl_plan_count(p.handle, 5, ctypes.byref(c)) == zl.ZL_ERR_INVALID_ARG
+    assert lib.zl_plan_count(p.handle, -1, ctypes.byref(c)) == zl.ZL_ERR_INVALID_ARG
     assert lib.zl_plan_count(None, 0, ctypes.byref(c)) == zl.ZL_ERR_INVALID_ARG
     assert lib.zl_plan_item(p.handle, len(w.items), None, None, None, None, None, None) == zl.ZL_ERR_INVALID_ARG
     assert lib.zl_plan_item(p.handle, -1, None, None, None, None, None, None) == zl.ZL_ERR_INVALID_ARG

@@ -62,3 +62,21 @@ def test_whole_sequences_land_packed_like_q():
     T, H, d = w.total_tokens, w.n_heads, w.head_dim
     o = r.bufs["o"][: T * H * d].reshape(T, H, d)
     assert np.isfinite(o).all()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n_members", [1, 3, 32, 33])
+def test_merge_group_sizes(d, n_members):
+    """k-split groups of 1 to 33 members (ragged chunk tails: 300 x 3 row-heads per member,
+    24 KV tokens each) beside a second, smaller group and a group whose members are all
+    empty (the merge's member loop in one pass up to 8 members, in batches beyond)."""
+    H, nq, ck = 3, 300, 24
+    L = max(nq, n_members * ck)
+    items = [WorkItem(0, L, 0, nq, 0, H, c * ck, (c + 1) * ck, 1) for c in range(n_members)]
+    items += [WorkItem(L, 200, 0, 150, 1, 3, 0, 90, 1), WorkItem(L, 200, 0, 150, 1, 3, 90, 200, 1)]
+    items += [WorkItem(L, 200, 10, 20, 0, 1, 0, 0, 1), WorkItem(L, 200, 10, 20, 0, 1, 5, 5, 1)]
+    w = Workload(f"kgroups{n_members}_d{d}", H, d, L + 200, items, d ** -0.5)
+    r = Run(w, seed=7)
+    r.check_forward()
+    empty = len(items) - 1
+    assert np.all(r.final_o(empty) == 0.0) and np.all(np.isneginf(r.final_lse(empty)))
