@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -103,11 +104,16 @@ def measured_peaks():
 
 def kernel_source_sha256(kernel: str) -> str:
     """Hash of a kernel's device code: its source file up to the host launcher (the
-    first `cudaError_t launch_` definition), so that a host-only change to the launch
-    does not void counters taken on the kernel."""
+    first `cudaError_t launch_` definition), with comments and blank lines removed, so
+    that neither a host-only change to the launch nor a comment voids counters taken on
+    the kernel."""
     text = open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb").read()
     cut = text.find(b"\ncudaError_t launch_")
-    return hashlib.sha256(text[:cut] if cut > 0 else text).hexdigest()
+    text = text[:cut] if cut > 0 else text
+    text = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+    text = re.sub(rb"//[^\n]*", b"", text)
+    text = b"\n".join(ln.rstrip() for ln in text.split(b"\n") if ln.strip())
+    return hashlib.sha256(text).hexdigest()
 
 
 def recorded_traffic(kernel: str):

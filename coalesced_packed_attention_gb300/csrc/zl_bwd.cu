@@ -28,7 +28,9 @@
 // they must overlap everything else.  Bulk reduce-adds from shared memory keep them out
 // of the sub-partitions' memory-instruction queues, where vector `red` instructions
 // (paced or not) held up the TMEM loads, MMA issues and TMA issues of the warps beside
-// them; the dQ reduction rate is what bounds the kernel on long items.
+// them.  On long items the kernel runs against the board's power cap: the bytes it moves
+// per FLOP (64 KB of reduce-adds and 64 KB of Q/dO per block pair) cost clock rate
+// more than any one stage stalls the block period.
 // Ordered dQ (plan flag ZL_PLAN_DETERMINISTIC_DQ; a separate instantiation, so the
 // default kernel carries none of it): the order in which CTAs reach a query block
 // decides the order of the fp32 additions, so by default dQ may change in its last bits

@@ -1,0 +1,40 @@
+"""Host helpers of bench.py: the device-code hash that keys committed DRAM counters."""
+import os
+import shutil
+
+import bench
+
+
+def _copy_tree(tmp_path, kernel):
+    rel = bench.KERNEL_SOURCES[kernel]
+    dst = tmp_path / rel
+    dst.parent.mkdir(parents=True)
+    shutil.copy(os.path.join(bench.ROOT, rel), dst)
+    (tmp_path / "profiles").mkdir()
+    src_prof = os.path.join(bench.ROOT, "profiles", f"{kernel}_training_traffic.txt")
+    if os.path.exists(src_prof):
+        shutil.copy(src_prof, tmp_path / "profiles")
+    return dst
+
+
+def test_hash_ignores_comments_not_code(tmp_path, monkeypatch):
+    kernel = "zl_bwd_main"
+    ref = bench.kernel_source_sha256(kernel)
+    dst = _copy_tree(tmp_path, kernel)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    text = dst.read_text()
+    dst.write_text("// a comment line\n" + text.replace("\n#include", "\n/* block\n comment */\n#include", 1))
+    assert bench.kernel_source_sha256(kernel) == ref
+    dst.write_text(text.replace("namespace zl {", "namespace zl {\nconstexpr int kUnused = 1;", 1))
+    assert bench.kernel_source_sha256(kernel) != ref
+
+
+def test_recorded_traffic_follows_the_device_code(tmp_path, monkeypatch):
+    kernel = "zl_bwd_main"
+    traffic = bench.recorded_traffic(kernel)
+    assert traffic is not None and traffic > 0  # counters taken on the current device code
+    dst = _copy_tree(tmp_path, kernel)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic(kernel) == traffic
+    dst.write_text(dst.read_text().replace("namespace zl {", "namespace zl {\nconstexpr int kUnused = 1;", 1))
+    assert bench.recorded_traffic(kernel) is None
