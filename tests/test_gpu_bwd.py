@@ -49,3 +49,28 @@ def test_whole_item_gradient_sums():
         s = it.seq_offset
         np.testing.assert_allclose(dv.sum(axis=0), r.do[s:s + it.seq_len].sum(axis=0), atol=5e-2)
         np.testing.assert_allclose(dk.sum(axis=0), 0.0, atol=5e-2)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_non_finite_tokens_outside_the_items(d):
+    """Tokens that belong to no item (gaps between and after the packed sequences) hold
+    NaN in Q, K, V and dO.  Every ragged tile reads such tokens next to its item (an
+    item's last KV block, its last query block), and the outputs must stay exactly
+    those of the oracle, which never reads them."""
+    from coalesced_packed_attention_gb300.workloads import WorkItem
+    H = 3
+    A, B = (0, 300), (400, 250)  # gaps [300, 400) and [650, 704)
+    items = [
+        WorkItem(A[0], A[1], 0, A[1], 0, H, 0, A[1], 0),     # whole A (ragged KV and query tails)
+        WorkItem(B[0], B[1], 0, B[1], 0, H, 0, B[1], 0),     # whole B
+        WorkItem(B[0], B[1], 0, 100, 0, H, 0, B[1], 0),      # q shard of B
+        WorkItem(A[0], A[1], 0, A[1], 0, 2, 0, 130, 1),      # k split of A, heads [0, 2):
+        WorkItem(A[0], A[1], 0, A[1], 0, 2, 130, A[1], 1),   # the second chunk ends at the gap
+    ]
+    w = Workload(f"gaps_d{d}", H, d, 704, items, d ** -0.5, with_backward=True)
+    r = Run(w, seed=9, backward=True, poison=[(300, 400), (650, 704)])
+    r.check_forward()
+    check_backward(r)
+    for i in range(len(items)):
+        for g in ("dq", "dk", "dv"):
+            assert np.isfinite(r.grad(i, g)).all(), (i, g)
