@@ -51,12 +51,13 @@ def test_whole_item_gradient_sums():
         np.testing.assert_allclose(dk.sum(axis=0), 0.0, atol=5e-2)
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_non_finite_tokens_outside_the_items(d):
+@pytest.mark.parametrize("d,flags", [(64, 0), (128, 0), (128, "fuse"), (128, "ordered")])
+def test_non_finite_tokens_outside_the_items(d, flags):
     """Tokens that belong to no item (gaps between and after the packed sequences) hold
     NaN in Q, K, V and dO.  Every ragged tile reads such tokens next to its item (an
     item's last KV block, its last query block), and the outputs must stay exactly
-    those of the oracle, which never reads them."""
+    those of the oracle, which never reads them; also with the k-split group fused into
+    the forward and with ordered dQ adds."""
     from coalesced_packed_attention_gb300.workloads import WorkItem
     H = 3
     A, B = (0, 300), (400, 250)  # gaps [300, 400) and [650, 704)
@@ -68,7 +69,9 @@ def test_non_finite_tokens_outside_the_items(d):
         WorkItem(A[0], A[1], 0, A[1], 0, 2, 130, A[1], 1),   # the second chunk ends at the gap
     ]
     w = Workload(f"gaps_d{d}", H, d, 704, items, d ** -0.5, with_backward=True)
-    r = Run(w, seed=9, backward=True, poison=[(300, 400), (650, 704)])
+    from coalesced_packed_attention_gb300 import zl
+    f = {0: 0, "fuse": zl.ZL_PLAN_FUSE_LOCAL_KMERGE, "ordered": zl.ZL_PLAN_DETERMINISTIC_DQ}[flags]
+    r = Run(w, seed=9, backward=True, flags=f, poison=[(300, 400), (650, 704)])
     r.check_forward()
     check_backward(r)
     for i in range(len(items)):
