@@ -518,8 +518,10 @@ def forward_config_numbers(dev, stream, steps, warmup, peak):
     """Forward (+ merge) TFLOP/s of the forward-only work lists: 64 whole images
     (48 x 256, 12 x 1024, 4 x 4096 tokens), and the 147600-token video as 8 k chunks
     beside 8 x 4096-token images, merged (fp32 partials + merge launch) and with the
-    k-split group fused into the forward (ZL_PLAN_FUSE_LOCAL_KMERGE).  Median of the
-    steps; the merge's GB/s from its algorithmic bytes."""
+    k-split group fused into the forward (ZL_PLAN_FUSE_LOCAL_KMERGE).  After the warm-up,
+    `steps` iterations or as many as fill ~50 ms (at most 200) run back to back, each
+    bracketed by events, with one synchronize at the end; median of them.  The merge's
+    GB/s from its algorithmic bytes."""
     import torch
     from coalesced_packed_attention_gb300 import zl
     from coalesced_packed_attention_gb300.workloads import config_images, config_long_video, make_inputs
@@ -531,17 +533,25 @@ def forward_config_numbers(dev, stream, steps, warmup, peak):
         q, k, v = make_inputs(T, H, d, seed=0, device=str(dev))[:3]
         plan = zl.zl_plan_worklist(work.items, H, d, T, flags)
         bufs = zl.allocate(plan, dev)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        times = []
-        for s_ in range(warmup + steps):
-            ev[0].record(stream)
+        def launch(evs):
+            evs[0].record(stream)
             zl.zl_coalesced_attn_fwd(plan, q, k, v, bufs["o"], bufs["o_partial"], bufs["lse"], scale, stream)
-            ev[1].record(stream)
+            evs[1].record(stream)
             zl.zl_merge_partials(plan, bufs["o_partial"], bufs["lse"], bufs["o"], bufs["lse"], stream)
-            ev[2].record(stream)
+            evs[2].record(stream)
+
+        warm = []
+        for _ in range(max(2, warmup)):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            launch(evs)
             torch.cuda.synchronize(dev)
-            if s_ >= warmup:
-                times.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
+            warm.append(evs[0].elapsed_time(evs[2]))
+        n = max(steps, min(200, int(50.0 / max(min(warm), 1e-3))))
+        evs_all = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for evs in evs_all:
+            launch(evs)
+        torch.cuda.synchronize(dev)
+        times = [(e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])) for e in evs_all]
         if zl.zl_get_device_status(plan, stream) != 0:
             raise RuntimeError(f"device status after {work.name}")
         f_ms = float(np.median([a for a, _ in times]))
@@ -555,7 +565,7 @@ def forward_config_numbers(dev, stream, steps, warmup, peak):
                 merge_bytes += len(members) * it.nq * it.nh * (4 * d + 4) + it.nq * it.nh * (2 * d + 4)
         tf = F / ((f_ms + m_ms) * 1e-3) / 1e12
         out.append({"workload": work.name, "kmerge": tag if plan.n_groups else None, "fwd_tflop": F / 1e12,
-                    "fwd_ms": f_ms, "merge_ms": m_ms, "tflops_fwd_plus_merge": tf,
+                    "iterations": n, "fwd_ms": f_ms, "merge_ms": m_ms, "tflops_fwd_plus_merge": tf,
                     "tflops_fwd": F / (f_ms * 1e-3) / 1e12, "frac_fwd_plus_merge": tf / peak,
                     "merge_gbs": merge_bytes / (m_ms * 1e-3) / 1e9 if merge_bytes and m_ms > 0 else None,
                     "fwd_tiles": plan.n_fwd_tiles})
