@@ -131,7 +131,7 @@ class Run:
     """One forward (+ merge, + backward) of a work list on cuda:0."""
 
     def __init__(self, work, seed=0, structured=False, backward=False, items=None, flags=0, groups=None,
-                 poison=()):
+                 poison=(), inputs=None):
         import torch
         ensure_library()
         self.work = work
@@ -139,7 +139,9 @@ class Run:
         H, d, T = work.n_heads, work.head_dim, work.total_tokens
         self.scale = work.scale
         self.relative = structured
-        ins = make_inputs(T, H, d, seed, with_grad_output=backward, structured=structured)
+        # inputs: given bf16 [T, H, d] CPU tensors (Q, K, V and, for a backward, dO), else seeded
+        ins = list(inputs) if inputs is not None else make_inputs(T, H, d, seed, with_grad_output=backward,
+                                                                   structured=structured)
         for lo, hi in poison:  # tokens of no item set to NaN in every input
             for x in ins:
                 x[lo:hi] = float("nan")

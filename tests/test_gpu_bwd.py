@@ -77,3 +77,40 @@ def test_non_finite_tokens_outside_the_items(d, flags):
     for i in range(len(items)):
         for g in ("dq", "dk", "dv"):
             assert np.isfinite(r.grad(i, g)).all(), (i, g)
+
+
+@pytest.mark.parametrize("name", ["worked_example.json", "worked_example_scale2.json"])
+def test_golden_worked_example_on_the_gpu(name):
+    """The hand-worked examples of tests/golden (one query over three keys, head dim 2,
+    score scale 1 and 2) through the CUDA forward and backward: the head dim is padded
+    with zeros to 64, which leaves every score, weight and LSE unchanged and the padded
+    output columns exactly zero.  Gates: the bf16 rounding of the stored O and of the
+    kernel's P and dS (at most a few 1e-3 on these O(0.1-1) values)."""
+    import json
+    import math
+    import os
+    import torch
+    from coalesced_packed_attention_gb300.workloads import WorkItem
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        g = json.load(f)
+    ns = {"e": math.e, "log": math.log, "exp": math.exp}
+    ev = lambda a: np.array([[eval(x, {}, ns) for x in r] for r in a])  # noqa: E731
+    T, d = 3, 64
+
+    def pad(rows):
+        x = torch.zeros(T, 1, d)
+        x[:len(rows), 0, :2] = torch.tensor(rows, dtype=torch.float32)
+        return x.to(torch.bfloat16)
+
+    q, k, v, do = pad(g["q"]), pad(g["k"]), pad(g["v"]), pad(g["do"])
+    w = Workload(f"golden_{name}", 1, d, T, [WorkItem(0, T, 0, 1, 0, 1, 0, 3, 0)], g["scale"], with_backward=True)
+    r = Run(w, backward=True, inputs=(q, k, v, do))
+    O, L = r.own_o(0)[:, 0, :], r.own_lse(0)[0]
+    np.testing.assert_allclose(L, [eval(x, {}, ns) for x in g["expected"]["lse"]], atol=1e-5)
+    np.testing.assert_allclose(O[:, :2], ev(g["expected"]["o"]), atol=5e-3)
+    dq, dk, dv = (r.grad(0, x)[:, 0, :] for x in ("dq", "dk", "dv"))
+    np.testing.assert_allclose(dq[:, :2], ev(g["expected"]["dq"]), atol=5e-3)
+    np.testing.assert_allclose(dk[:, :2], ev(g["expected"]["dk"]), atol=5e-3)
+    np.testing.assert_allclose(dv[:, :2], ev(g["expected"]["dv"]), atol=5e-3)
+    for x in (O, dq, dk, dv):
+        assert np.all(x[:, 2:] == 0.0)
