@@ -114,3 +114,49 @@ def test_golden_worked_example_on_the_gpu(name):
     np.testing.assert_allclose(dv[:, :2], ev(g["expected"]["dv"]), atol=5e-3)
     for x in (O, dq, dk, dv):
         assert np.all(x[:, 2:] == 0.0)
+
+
+def test_closed_forms_on_the_gpu():
+    """Closed forms of exact attention through the CUDA forward and backward, with no
+    oracle in between.  Three sequences, d = 128, 2 heads:
+    A (300 tokens, Q = 0): P is uniform, so O = mean of V over the chunk, LSE = ln 300,
+      dK = 0 exactly (every term carries a Q row) and every dV row = (sum of dO) / 300;
+    B (a single key, KV [7, 8)): P = 1, so O = V_7 exactly, LSE = scale q.k_7, dS = 0
+      (dQ = dK = 0 up to rounding) and dV_7 = sum of dO over the rows;
+    C (V = 0.5 everywhere): O = 0.5, dS = 0 (dP = D), so dQ = dK = 0 up to rounding."""
+    import torch
+    from coalesced_packed_attention_gb300.workloads import WorkItem, make_inputs
+    H, d = 2, 128
+    A, B, C = (0, 300), (300, 256), (556, 256)
+    T = 812
+    q, k, v, do = make_inputs(T, H, d, seed=11, with_grad_output=True)
+    q[A[0]:A[0] + A[1]] = 0
+    v[C[0]:C[0] + C[1]] = 0.5
+    items = [WorkItem(A[0], A[1], 0, A[1], 0, H, 0, A[1], 0),
+             WorkItem(B[0], B[1], 0, B[1], 0, H, 7, 8, 0),
+             WorkItem(C[0], C[1], 0, C[1], 0, H, 0, C[1], 0)]
+    scale = d ** -0.5
+    w = Workload("closed_forms", H, d, T, items, scale, with_backward=True)
+    r = Run(w, backward=True, inputs=(q, k, v, do))
+    qf, kf, vf, dof = (x.double().numpy() for x in (q, k, v, do))
+    # A: uniform weights
+    sa = slice(A[0], A[0] + A[1])
+    np.testing.assert_allclose(r.own_lse(0), np.log(A[1]), atol=1e-5)
+    np.testing.assert_allclose(r.own_o(0), np.broadcast_to(vf[sa].mean(axis=0), (A[1], H, d)), atol=2e-3)
+    assert np.all(r.grad(0, "dk") == 0.0)
+    np.testing.assert_allclose(r.grad(0, "dv"), np.broadcast_to(dof[sa].sum(axis=0) / A[1], (A[1], H, d)),
+                               atol=2e-3)
+    # B: one key
+    sb = slice(B[0], B[0] + B[1])
+    assert np.array_equal(r.own_o(1), np.broadcast_to(vf[B[0] + 7], (B[1], H, d)))
+    s7 = scale * np.einsum("rhd,hd->hr", qf[sb], kf[B[0] + 7])
+    np.testing.assert_allclose(r.own_lse(1), s7, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(r.grad(1, "dq"), 0.0, atol=1e-3)
+    np.testing.assert_allclose(r.grad(1, "dk"), 0.0, atol=1e-3)
+    np.testing.assert_allclose(r.grad(1, "dv")[0], dof[sb].sum(axis=0), rtol=1e-4, atol=1e-3)
+    # C: constant values
+    # (the stored bf16 O may round 0.5 - 1e-3 down one step, which leaves dP - D at a
+    # few 1e-3 of sum |dO| and dQ, dK at ~1e-4)
+    np.testing.assert_allclose(r.own_o(2), 0.5, atol=2e-3)
+    np.testing.assert_allclose(r.grad(2, "dq"), 0.0, atol=5e-3)
+    np.testing.assert_allclose(r.grad(2, "dk"), 0.0, atol=5e-3)
