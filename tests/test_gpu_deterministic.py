@@ -79,3 +79,27 @@ def test_repeated_backward_is_bitwise_identical(make):
     for o in outs[1:]:
         for key in ("dq", "dk", "dv"):
             np.testing.assert_array_equal(o[key], outs[0][key], err_msg=key)
+
+
+def test_shards_reproduce_the_whole_gradients_bit_for_bit():
+    """With ordered dQ adds every dQ element sums its KV tiles in tile order, and every
+    tile walks the query blocks from the first, so a q-shard's dQ rows and an h-shard's
+    dQ, dK and dV equal the whole item's bit for bit (a query row's dS and its dQ terms
+    involve only that row; the shards' O and LSE equal the whole's bit for bit too)."""
+    H, d, L = 4, 128, 1000
+    items = [WorkItem(0, L, 0, L, 0, H, 0, L, 0),        # whole
+             WorkItem(0, L, 0, 300, 0, H, 0, L, 0),      # q shards at unaligned boundaries
+             WorkItem(0, L, 300, 777, 0, H, 0, L, 0),
+             WorkItem(0, L, 777, L, 0, H, 0, L, 0),
+             WorkItem(0, L, 0, L, 0, 1, 0, L, 0),        # h shards
+             WorkItem(0, L, 0, L, 1, H, 0, L, 0)]
+    w = Workload("shards_bitwise_bwd", H, d, L, items, d ** -0.5, with_backward=True)
+    r = Run(w, seed=13, backward=True, flags=DET)
+    dq, dk, dv = (r.grad(0, x) for x in ("dq", "dk", "dv"))
+    for i in (1, 2, 3):
+        it = items[i]
+        assert np.array_equal(r.grad(i, "dq"), dq[it.q_lo:it.q_hi]), i
+    for i in (4, 5):
+        it = items[i]
+        for name, whole in (("dq", dq), ("dk", dk), ("dv", dv)):
+            assert np.array_equal(r.grad(i, name), whole[:, it.h_lo:it.h_hi]), (i, name)

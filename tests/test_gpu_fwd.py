@@ -80,3 +80,23 @@ def test_merge_group_sizes(d, n_members):
     r.check_forward()
     empty = len(items) - 1
     assert np.all(r.final_o(empty) == 0.0) and np.all(np.isneginf(r.final_lse(empty)))
+
+
+def test_shards_reproduce_the_whole_bit_for_bit():
+    """Query rows and heads are computed independently (a row's scores, weights and
+    rescales involve only that row; a warp's shared rescale vote multiplies rows that
+    need none by exactly 1), so q-shards at unaligned boundaries and h-shards of a
+    sequence give exactly the whole item's O and LSE."""
+    H, d, L = 4, 128, 1000
+    items = [WorkItem(0, L, 0, L, 0, H, 0, L, 0),        # whole
+             WorkItem(0, L, 0, 300, 0, H, 0, L, 0),      # q shards: [0,300) [300,777) [777,1000)
+             WorkItem(0, L, 300, 777, 0, H, 0, L, 0),
+             WorkItem(0, L, 777, L, 0, H, 0, L, 0),
+             WorkItem(0, L, 0, L, 0, 1, 0, L, 0),        # h shards: {0}, {1, 2, 3}
+             WorkItem(0, L, 0, L, 1, H, 0, L, 0)]
+    w = Workload("shards_bitwise", H, d, L, items, d ** -0.5)
+    r = Run(w, seed=12)
+    O, lse = r.own_o(0), r.own_lse(0)
+    for i, it in enumerate(items[1:], start=1):
+        assert np.array_equal(r.own_o(i), O[it.q_lo:it.q_hi, it.h_lo:it.h_hi]), i
+        assert np.array_equal(r.own_lse(i), lse[it.h_lo:it.h_hi, it.q_lo:it.q_hi]), i
