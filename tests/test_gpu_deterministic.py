@@ -103,3 +103,23 @@ def test_shards_reproduce_the_whole_gradients_bit_for_bit():
         it = items[i]
         for name, whole in (("dq", dq), ("dk", dk), ("dv", dv)):
             assert np.array_equal(r.grad(i, name), whole[:, it.h_lo:it.h_hi]), (i, name)
+
+
+def test_co_location_leaves_results_unchanged():
+    """Co-location changes the schedule, not the result (pith.science review, "What
+    carries the argument": whole sequences and shards share one launch): an image, the
+    video's q shard and its k shard give the same O and LSE bit for bit whether each runs
+    alone or coalesced with the other 19 items, and (with ordered dQ adds) the same dQ,
+    dK and dV for the image and the q shard."""
+    w = scaled(config_training(), 12)
+    full = Run(w, seed=14, backward=True, flags=DET)
+    picks = [0, w.labels.index("video_qsplit"), w.labels.index("video_ksplit")]
+    for i in picks:
+        it = w.items[i]
+        alone = Run(Workload(f"alone_{i}", w.n_heads, w.head_dim, w.total_tokens, [it], w.scale,
+                             with_backward=True), seed=14, backward=True, flags=DET)
+        assert np.array_equal(alone.own_o(0), full.own_o(i)), i
+        assert np.array_equal(alone.own_lse(0), full.own_lse(i)), i
+        if not it.emit_lse:  # a k shard alone has no partner to merge with
+            for name in ("dq", "dk", "dv"):
+                assert np.array_equal(alone.grad(0, name), full.grad(i, name)), (i, name)
