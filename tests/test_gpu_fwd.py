@@ -100,3 +100,17 @@ def test_shards_reproduce_the_whole_bit_for_bit():
     for i, it in enumerate(items[1:], start=1):
         assert np.array_equal(r.own_o(i), O[it.q_lo:it.q_hi, it.h_lo:it.h_hi]), i
         assert np.array_equal(r.own_lse(i), lse[it.h_lo:it.h_hi, it.q_lo:it.q_hi]), i
+
+
+def test_merge_with_an_empty_chunk_is_the_unsplit_item_bit_for_bit():
+    """A k-split group of the full KV range and an empty chunk: the empty chunk's LSE is
+    -inf, so the merge's weight is exp(0) = 1 and its LSE is the full chunk's exactly, and
+    the merged O and LSE equal the unsplit item's bit for bit."""
+    H, d, L = 3, 128, 500
+    items = [WorkItem(0, L, 0, L, 0, H, 0, L, 0),       # unsplit
+             WorkItem(0, L, 0, L, 0, H, 0, L, 1),       # full chunk, emit_lse
+             WorkItem(0, L, 0, L, 0, H, L, L, 1)]       # empty chunk, same group
+    w = Workload("merge_empty_chunk", H, d, L, items, d ** -0.5)
+    r = Run(w, seed=15)
+    assert np.array_equal(r.final_o(1), r.own_o(0))
+    assert np.array_equal(r.final_lse(1), r.own_lse(0))
