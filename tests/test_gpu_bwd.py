@@ -22,6 +22,16 @@ def test_training_list_scaled_all_rows():
     check_backward(r)
 
 
+def test_training_list_scaled_all_rows_d64():
+    """The same mix of item kinds (whole images; q, h and k shards of the video, merged)
+    at head dim 64, forward and backward on all rows."""
+    import dataclasses
+    w = dataclasses.replace(scaled(config_training(), 12), head_dim=64, scale=64 ** -0.5)
+    r = Run(w, seed=16, backward=True)
+    r.check_forward()
+    check_backward(r)
+
+
 def test_training_list_scaled_structured():
     w = scaled(config_training(), 24)
     r = Run(w, seed=1, structured=True, backward=True)
