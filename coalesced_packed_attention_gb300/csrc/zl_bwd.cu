@@ -70,13 +70,15 @@ struct BwdLayout {
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;             // 2 stages
-  static constexpr int kDO = kQ + 2 * kTile;        // 1 stage (free once dV has read it)
+  static constexpr int kDO = kQ + 2 * kTile;        // 1 stage (free once dV has read it); ordered dQ
+                                                    // adds use the staging region as a 2nd stage
   static constexpr int kDS = kDO + kTile;           // [128 kv][128 q] bf16, two 128-byte-swizzled boxes
   static constexpr int kStageBytes = 128 * 32 * 4;  // one 32-column chunk of a block's dQ, fp32
   static constexpr int kStage = kDS + 2 * kBox;     // 2 staging buffers of the dQ drain
   static constexpr int kLD = kStage + 2 * kStageBytes;  // [2 block parities] LSE*log2(e) and D of a block's 128 queries
   static constexpr int kBar = kLD + 2 * 2 * 128 * 4;
-  static constexpr int kNumBars = 25;
+  static constexpr int kNumBars = 27;
+  static_assert(2 * kStageBytes >= kTile && kStage % 1024 == 0, "second dO stage does not fit the staging region");
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 64;
 };
@@ -225,6 +227,13 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
   uint64_t* dp_full = bar + 20;   // dP^T of the block in TMEM R1
   uint64_t* stage_full = bar + 21;  // [2] a dQ chunk written to staging buffer b (128 arrivals)
   uint64_t* stage_free = bar + 23;  // [2] the bulk reduce-add of buffer b has read it
+  // dO stages: one (default), or two with ordered dQ adds, whose drain needs no staging
+  // buffers (the second stage takes their place): block qit's dO is in stage dst_of(qit)
+  constexpr uint32_t kDOStages = kOrdered ? 2 : 1;
+  auto do_stage = [](uint32_t qit) { return kDOStages == 2 ? (qit & 1) : 0u; };
+  auto do_phase = [](uint32_t qit) { return kDOStages == 2 ? ((qit >> 1) & 1) : (qit & 1); };
+  auto do_full_s = [&](uint32_t st) { return st ? bar + 25 : do_full; };
+  auto do_empty_s = [&](uint32_t st) { return st ? bar + 26 : do_empty; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   uint32_t* tmem_slot = misc;
   volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(misc + 2);
@@ -247,8 +256,10 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
       mbar_init(tile_full + i, 1);
       mbar_init(tile_empty + i, 1 + 8 + 4);
     }
-    mbar_init(do_full, 1);
-    mbar_init(do_empty, 1);
+    for (uint32_t i = 0; i < 2; ++i) {
+      mbar_init(do_full_s(i), 1);
+      mbar_init(do_empty_s(i), 1);
+    }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 256);
@@ -278,6 +289,7 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
   uint8_t* sV = smem + L::kV;
   uint8_t* sQ = smem + L::kQ;
   uint8_t* sDO = smem + L::kDO;
+  auto sDO_s = [&](uint32_t st) { return st ? smem + L::kStage : sDO; };
   uint8_t* sDS = smem + L::kDS;
 
   if (warp >= 12) {
@@ -325,11 +337,12 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           for (int c = 0; c < D / 64; ++c)
             tma_load_3d(sQ + st * L::kTile + c * L::kBox, &tm_q, q_full + st, 64 * c, tl.head,
                         (int)it.seq_offset + it.q_lo + ib * kBlockM);
-          // one dO slot: block qit's dO waits until dV of block qit - 1 has read the slot
-          if (!bwait(do_empty, (qit & 1) ^ 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(do_full, L::kTile);
+          // block qit's dO waits until dV of the block that last used its stage has read it
+          const uint32_t dst = do_stage(qit), dph = do_phase(qit);
+          if (!bwait(do_empty_s(dst), dph ^ 1, abort_flag, p.wait_limit, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(do_full_s(dst), L::kTile);
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sDO + c * L::kBox, tm_do, do_full, 64 * c, hl, ib * kBlockM);
+            tma_load_3d(sDO_s(dst) + c * L::kBox, tm_do, do_full_s(dst), 64 * c, hl, ib * kBlockM);
           ++qit;
         }
       }
@@ -354,6 +367,8 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
       const uint32_t kK = sdesc_lo(aK, 16), kV = sdesc_lo(aV, 16), kQ = sdesc_lo(aQ, 16), kDO = sdesc_lo(aDO, 16);
       const uint32_t kDS = sdesc_lo(aDS, 16);
       const uint32_t mK = sdesc_lo(aK, L::kBox), mQ = sdesc_lo(aQ, L::kBox), mDO = sdesc_lo(aDO, L::kBox);
+      const uint32_t aDO1 = smem_u32(sDO_s(1));
+      const uint32_t kDO1 = sdesc_lo(aDO1, 16), mDO1 = sdesc_lo(aDO1, L::kBox);
       const uint32_t mDS = sdesc_lo(aDS, L::kBox);
       auto dsc = [](uint32_t lo, uint32_t bytes) { return sdesc_join(lo + (bytes >> 4)); };
       uint32_t tile_it = 0, kt = 0, qit = 0, nblocks = 0;
@@ -410,13 +425,15 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
         issue_s(qit & 1);
         for (int is = 0; is < nqb; ++is) {
           const uint32_t st = qit & 1;
-          if (!wait_w(do_full, qit & 1)) { ok = false; break; }
+          const uint32_t dst = do_stage(qit);
+          if (!wait_w(do_full_s(dst), do_phase(qit))) { ok = false; break; }
+          const uint32_t kDOb = dst ? kDO1 : kDO, mDOb = dst ? mDO1 : mDO;
           if (nblocks > 0 && !wait_w(dq_empty, (nblocks - 1) & 1)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
             const uint32_t off = (kk >> 2) * L::kBox + (kk & 3) * 32;
-            mma_ss_w(tR1, dsc(kV, off), dsc(kDO, off), kIdSq, kk > 0);
+            mma_ss_w(tR1, dsc(kV, off), dsc(kDOb, off), kIdSq, kk > 0);
           }
           mma_commit_w(dp_full);
           // dV += P^T dO as soon as P^T is in TMEM (the warpgroup then forms dS^T)
@@ -424,8 +441,8 @@ __global__ void __launch_bounds__(512, 1) zl_bwd_kernel(const __grid_constant__ 
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // K = 128 queries
-            mma_ts_w(tdV, tR0 + pcol(kk), dsc(mDO, kk * 2048), kIdKV, (is > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_w(do_empty);  // the producer may load the next block's dO
+            mma_ts_w(tdV, tR0 + pcol(kk), dsc(mDOb, kk * 2048), kIdKV, (is > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_w(do_empty_s(dst));  // the producer may load a later block's dO into the stage
           if (is + 1 < nqb) {
             // S^T of the next block as soon as dV has read P^T out of R0 (one thread's
             // products run in issue order): the softmax warpgroups start on it while
