@@ -46,7 +46,8 @@
 // claimed earlier (held by running CTAs), which rules out a cycle of waits.
 // TMEM (512 columns): R0 [0,128) S^T / P^T, R1 [128,256) dP^T / dQ, dV [256,256+d),
 // dK [384,384+d).  Shared memory: K, V, Q (2 stages), dO (1 stage: free once dV has read
-// it), dS^T, and two 16 KB dQ staging buffers.
+// it), dS^T, and two 16 KB dQ staging buffers; with ordered dQ adds, which stage nothing,
+// their 32 KB hold a second dO stage.
 // Warps: 0-7 softmax (two warpgroups), 8-11 dQ drain, 12 TMA producer, 13 MMA issuer,
 // 14-15 idle.  The block is launched with 128 registers per thread (16 warps: four per
 // SM sub-partition, 16K registers each) and the warpgroups then trade registers with
