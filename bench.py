@@ -75,7 +75,9 @@ def sample_clocks(stop: threading.Event, out: list):
 
 
 def summarize_clocks(lines, gpu_index):
-    sm, mx, reasons = [], None, set()
+    """Median SM clock and board power over the samples, the maximum SM clock, and every
+    throttle reason seen active."""
+    sm, pw, mx, reasons = [], [], None, set()
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     for ln in lines:
         f = [x.strip() for x in ln.split(",")]
@@ -86,12 +88,17 @@ def summarize_clocks(lines, gpu_index):
             mx = float(f[2])
         except ValueError:
             continue
+        try:
+            pw.append(float(f[3]))
+        except ValueError:
+            pass
         for n, v in zip(names, f[5:9]):
             if v.lower() == "active":
                 reasons.add(n)
     if not sm:
         return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
-    return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+    return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+            "power_w": float(np.median(pw)) if pw else None}
 
 
 def measured_peaks():

@@ -38,3 +38,14 @@ def test_recorded_traffic_follows_the_device_code(tmp_path, monkeypatch):
     assert bench.recorded_traffic(kernel) == 123456.0
     dst.write_text(dst.read_text().replace("namespace zl {", "namespace zl {\nconstexpr int kUnused = 1;", 1))
     assert bench.recorded_traffic(kernel) is None
+
+
+def test_clock_summary_reads_clock_power_and_reasons():
+    lines = ["0, 1942, 2070, 1385.2, 0x4, Not Active, Not Active, Not Active, Active",
+             "0, 1900, 2070, 1399.8, 0x4, Not Active, Not Active, Not Active, Active",
+             "1, 345, 2070, 60.0, 0x0, Active, Not Active, Not Active, Not Active",  # another GPU
+             "garbage"]
+    c = bench.summarize_clocks(lines, 0)
+    assert c == {"sm_mhz": 1921.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2,
+                 "power_w": 1392.5}
+    assert bench.summarize_clocks([], 0)["samples"] == 0
