@@ -56,7 +56,9 @@ def aggregate(total_ms, ws: int, flops_per_rank: float, steps: int):
 
 
 def sample_clocks(stop: threading.Event, out: list):
-    q = ("--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    # power.draw.instant: power.draw is a windowed average that blends in the idle time
+    # around a timed region shorter than its window
+    q = ("--query-gpu=index,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     try:
@@ -75,8 +77,8 @@ def sample_clocks(stop: threading.Event, out: list):
 
 
 def summarize_clocks(lines, gpu_index):
-    """Median SM clock and board power over the samples, the maximum SM clock, and every
-    throttle reason seen active."""
+    """Median SM clock and instantaneous board power over the samples, the maximum SM
+    clock, and every throttle reason seen active."""
     sm, pw, mx, reasons = [], [], None, set()
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     for ln in lines:
