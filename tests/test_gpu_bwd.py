@@ -170,3 +170,28 @@ def test_closed_forms_on_the_gpu():
     np.testing.assert_allclose(r.own_o(2), 0.5, atol=2e-3)
     np.testing.assert_allclose(r.grad(2, "dq"), 0.0, atol=5e-3)
     np.testing.assert_allclose(r.grad(2, "dk"), 0.0, atol=5e-3)
+
+
+def test_k_split_gradients_assemble_the_unsplit_item():
+    """A k split of theta (pith.science review, "What carries the argument"): each chunk
+    writes its contribution to dQ and the final dK, dV of its own KV rows, all with the
+    group's merged LSE and O.  So the chunks' dQ sum to the unsplit item's dQ, and their
+    dK, dV are the unsplit item's rows of their chunks, up to the bf16 rounding of the
+    stored O that enters D (the merged O and the unsplit item's O may differ by one bf16
+    step): a few 1e-3 at most, where a chunk that used its own LSE, or dropped one, would
+    be off by tens of percent."""
+    from coalesced_packed_attention_gb300.workloads import WorkItem
+    H, d, L = 3, 128, 700
+    cuts = [0, 130, 400, L]  # three uneven, unaligned chunks
+    items = [WorkItem(0, L, 0, L, 0, H, 0, L, 0)]
+    items += [WorkItem(0, L, 0, L, 0, H, a, b, 1) for a, b in zip(cuts, cuts[1:])]
+    w = Workload("k_split_assembly", H, d, L, items, d ** -0.5, with_backward=True)
+    r = Run(w, seed=17, backward=True)
+    def close(got, ref):
+        np.testing.assert_allclose(got, ref, rtol=0, atol=5e-3)
+        assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref)
+
+    close(sum(r.grad(i, "dq") for i in range(1, len(items))), r.grad(0, "dq"))
+    for i, (a, b) in enumerate(zip(cuts, cuts[1:]), start=1):
+        for name in ("dk", "dv"):
+            close(r.grad(i, name), r.grad(0, name)[a:b])
