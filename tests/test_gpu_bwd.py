@@ -195,3 +195,22 @@ def test_k_split_gradients_assemble_the_unsplit_item():
     for i, (a, b) in enumerate(zip(cuts, cuts[1:]), start=1):
         for name in ("dk", "dv"):
             close(r.grad(i, name), r.grad(0, name)[a:b])
+
+
+def test_q_split_partial_gradients_sum_to_the_unsplit_item():
+    """A q split of theta: each shard writes dQ for its own rows and partial dK, dV (its
+    rows' contribution, which a distributed run would reduce).  The shards' O and LSE are
+    the whole item's bit for bit, so their partial dK, dV sum to the whole item's and their
+    dQ rows are the whole item's, up to fp32 summation order only."""
+    from coalesced_packed_attention_gb300.workloads import WorkItem
+    H, d, L = 3, 128, 1000
+    cuts = [0, 300, 777, L]
+    items = [WorkItem(0, L, 0, L, 0, H, 0, L, 0)]
+    items += [WorkItem(0, L, a, b, 0, H, 0, L, 0) for a, b in zip(cuts, cuts[1:])]
+    w = Workload("q_split_assembly", H, d, L, items, d ** -0.5, with_backward=True)
+    r = Run(w, seed=18, backward=True)
+    for name in ("dk", "dv"):
+        np.testing.assert_allclose(sum(r.grad(i, name) for i in range(1, len(items))), r.grad(0, name),
+                                   rtol=1e-5, atol=1e-5)
+    for i, (a, b) in enumerate(zip(cuts, cuts[1:]), start=1):
+        np.testing.assert_allclose(r.grad(i, "dq"), r.grad(0, "dq")[a:b], rtol=1e-5, atol=1e-5)
